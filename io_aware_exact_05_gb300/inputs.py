@@ -1,0 +1,89 @@
+"""Seeded synthetic inputs for the five attention workloads.
+
+This module holds no attention arithmetic: it only draws Gaussian Q, K, V and
+dO from a seeded CPU generator, rounds them to the workload's dtype and
+(optionally) moves them to a device.  Both the CUDA path and the float64
+oracle are fed from here, so the two see bit-identical inputs.
+
+Workloads (batch B, heads H, sequence n, head dim d):
+
+  tiny_f32        B1  H1  n128   d64   fp32  non-causal  N(0,1)
+  b4h16_n2k_d64   B4  H16 n2048  d64   bf16  non-causal  N(0,1)
+  b2h16_n8k_d128  B2  H16 n8192  d128  bf16  causal      N(0,1)
+  b1h8_n32k_d128  B1  H8  n32768 d128  bf16  causal      Q,K ~ N(0,4); V,dO ~ N(0,1)
+  b2h8_n4k_d256   B2  H8  n4096  d256  bf16  non-causal  N(0,1)
+
+Values are drawn in float32 and rounded to bf16 round-to-nearest-even; the
+Q/K factor 2.0 of the sharp-softmax workload is a power of two, so it is
+exact in either dtype.
+"""
+
+from dataclasses import dataclass, replace
+
+import torch
+
+__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs"]
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    n: int
+    d: int
+    dtype: str          # "bf16" or "f32"
+    causal: bool
+    qk_gain: float = 1.0
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def scale(self):
+        return 1.0 / float(self.d) ** 0.5
+
+    def with_shape(self, **kw):
+        """A copy with some fields replaced (used for ragged/small variants)."""
+        return replace(self, **kw)
+
+
+WORKLOADS = [
+    Workload("tiny_f32", 1, 1, 128, 64, "f32", False, 1.0, 1001),
+    Workload("b4h16_n2k_d64", 4, 16, 2048, 64, "bf16", False, 1.0, 1002),
+    Workload("b2h16_n8k_d128", 2, 16, 8192, 128, "bf16", True, 1.0, 1003),
+    Workload("b1h8_n32k_d128", 1, 8, 32768, 128, "bf16", True, 2.0, 1004),
+    Workload("b2h8_n4k_d256", 2, 8, 4096, 256, "bf16", False, 1.0, 1005),
+]
+
+
+def workload(name):
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def make_inputs(w, device="cpu", pin=False):
+    """Draw q, k, v, do of shape (B, H, n, d) for workload ``w``.
+
+    Draw order is fixed (q, k, v, do) from ``torch.Generator().manual_seed(w.seed)``.
+    Returns a dict of tensors in ``w.torch_dtype`` on ``device`` (pinned host
+    memory if ``pin`` and device is cpu).
+    """
+    g = torch.Generator(device="cpu").manual_seed(int(w.seed))
+    shape = (w.B, w.H, w.n, w.d)
+    out = {}
+    for name in ("q", "k", "v", "do"):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if name in ("q", "k") and w.qk_gain != 1.0:
+            x.mul_(w.qk_gain)
+        x = x.to(w.torch_dtype)
+        if device != "cpu":
+            x = x.to(device)
+        elif pin:
+            x = x.pin_memory()
+        out[name] = x
+    return out
