@@ -1,0 +1,369 @@
+#!/usr/bin/env python
+"""Throughput of exact attention forward + backward on GB300 through libattn.
+
+One step = one forward (attn_fwd) and one backward (attn_bwd_preprocess,
+attn_bwd_dkdv, attn_bwd_dq) over the whole workload, inputs resident in HBM.
+Throughput counts the algorithmic FLOPs (forward 4*B*H*n^2*d, backward
+10*B*H*n^2*d, both halved for a causal mask).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--mode atomic|pass] [--impl ours|reference]
+
+Under torchrun each rank runs its own copy of the workload on its GPU (every
+(b, h) head is independent, so there is no collective on the data path:
+weak scaling); the timed region is bracketed by barriers and the maximum
+elapsed time over ranks is reported.  --impl reference times the float64 CPU
+oracle on the host cores instead (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from io_aware_exact_05_gb300.flops import attention_flops  # noqa: E402
+from io_aware_exact_05_gb300.inputs import make_inputs, workload  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "b2h16_n8k_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------ reference arm
+def oracle_step(w, x, heads, n_sub=None):
+    """Float64 CPU oracle forward + backward over the given heads, on the
+    first n_sub tokens of each (the whole head by default)."""
+    import oracle
+
+    m = w.n if n_sub is None else n_sub
+    q, k, v, do = (x[n].reshape(w.B * w.H, w.n, w.d) for n in ("q", "k", "v", "do"))
+    for h in heads:
+        oracle.attention_forward_head(q[h][:m], k[h][:m], v[h][:m], w.scale, w.causal)
+        oracle.attention_backward_head(q[h][:m], k[h][:m], v[h][:m], do[h][:m], w.scale,
+                                       w.causal)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def time_oracle(w, x, budget_s=12.0, max_heads=4):
+    """Time the oracle on whole heads until ~budget_s of CPU work."""
+    heads, t = [], 0.0
+    for h in range(min(max_heads, w.B * w.H)):
+        t0 = time.perf_counter()
+        oracle_step(w, x, [h])
+        t += time.perf_counter() - t0
+        heads.append(h)
+        if t >= budget_s:
+            break
+    f = attention_flops(1, len(heads), w.n, w.d, w.causal)["total"]
+    return {"value": f / t / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": "float64 numpy oracle, forward+backward of %d of %d whole heads of %s "
+                      "(%.1f s)" % (len(heads), w.B * w.H, w.name, t)}
+
+
+def run_reference(args, w):
+    """The float64 oracle on the host cores.  One step = forward + backward of
+    the first n_sub tokens of one head, n_sub chosen from a calibration run so
+    that warm-up + timed steps take about 90 s in total."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    x = make_inputs(w)
+    cal = min(1024, w.n)
+    t0 = time.perf_counter()
+    oracle_step(w, x, [0], cal)
+    t_cal = max(time.perf_counter() - t0, 1e-3)
+    target = min(5.0, 90.0 / max(1, args.steps + args.warmup))
+    n_sub = int(round(cal * (target / t_cal) ** 0.5 / 128)) * 128
+    n_sub = max(128, min(w.n, n_sub))
+    per_step = attention_flops(1, 1, n_sub, w.d, w.causal)["total"]
+    for i in range(args.warmup):
+        oracle_step(w, x, [i % (w.B * w.H)], n_sub)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle_step(w, x, [s % (w.B * w.H)], n_sub)
+    el = time.perf_counter() - t0
+    val = per_step * args.steps / el / 1e12
+    sample = ("forward+backward of the first %d of %d tokens of one head (d=%d, %s) per step, "
+              "float64 numpy oracle" % (n_sub, w.n, w.d, "causal" if w.causal else "full"))
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("bwd_tc.cu", "sm100.cuh"):
+        h.update(open(os.path.join(ROOT, "io_aware_exact_05_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "bwd_dkdv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch_full_workload")
+
+
+def run_ours(args, w):
+    from io_aware_exact_05_gb300 import attn
+
+    ws_n, rank, local = dist_env()
+    dist = ws_n > 1
+    if dist:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mode = {"atomic": attn.ATTN_DQ_ATOMIC, "pass": attn.ATTN_DQ_PASS,
+            "auto": attn.ATTN_DQ_AUTO}[args.mode]
+    wr = w.with_shape(seed=w.seed + 7919 * rank)    # each rank its own batch
+    x = make_inputs(wr)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = attn.attn_bwd_workspace_size(w.B, w.H, w.n, w.d, attn.ATTN_BF16, w.causal, mode)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+    sc = w.scale
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e: e[0].record(st)
+        attn.attn_fwd(q, k, v, o, lse, sc, w.causal, st)
+        if e: e[1].record(st)
+        attn.attn_bwd_preprocess(o, do, lse, w.causal, mode, work, st)
+        if e: e[2].record(st)
+        attn.attn_bwd_dkdv(q, k, v, do, dk, dv, sc, w.causal, mode, work, st)
+        if e: e[3].record(st)
+        attn.attn_bwd_dq(q, k, v, do, dq, sc, w.causal, mode, work, st)
+        if e: e[4].record(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after warm-up: " + attn.attn_strerror(rc))
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for i in range(args.steps):
+        step(ev[i])
+    t1.record(st)
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    clk = clocks.stop()
+    el_ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([el_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        el_ms = float(tt.item())
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after timing: " + attn.attn_strerror(rc))
+    stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(args.steps)) / args.steps
+                for s in range(4)]
+
+    fl = attention_flops(w.B, w.H, w.n, w.d, w.causal)
+    per_step = fl["total"]
+    value = per_step * ws_n * args.steps / (el_ms * 1e-3) / 1e12
+    pk, src = peaks()
+
+    # ---- end to end through the public API with host buffers
+    hx = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    ho = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+          for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        for n_, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(hx[n_], non_blocking=True)
+        step()
+        for n_, src_ in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            ho[n_].copy_(src_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        kv_ms = stage_ms[2]
+        achieved = fl["bwd"] / (kv_ms * 1e-3) / 1e12
+        peak = float(pk["bf16_tflops"])
+        tr = traffic_per_launch()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "pct_of_peak": 100.0 * value / ws_n / peak,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
+                       "causal": w.causal, "dq_mode": args.mode,
+                       "parallelism": "replicas x%d (heads independent)" % ws_n,
+                       "l2": "inputs larger than L2: Q,K,V,dO = %.0f MB per GPU vs 126 MB L2"
+                             % (h2d / 1e6)},
+            "stage_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1],
+                         "bwd_dkdv": stage_ms[2], "bwd_dq": stage_ms[3]},
+            "tflops": {"fwd": fl["fwd"] / (stage_ms[0] * 1e-3) / 1e12,
+                       "bwd": fl["bwd"] / (sum(stage_ms[1:]) * 1e-3) / 1e12},
+            "roofline": {"kernel": "bwd_kv_kernel (attn_bwd_dkdv)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": tr,
+                         "peak_source": "%s bf16_tflops (burst); sustained %s" % (
+                             src, pk.get("bf16_tflops_sustained"))},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and ws_n == 1:
+            line["cpu_baseline"] = time_oracle(w, x)
+        print(json.dumps(line), flush=True)
+    if dist:
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", default="atomic", choices=["atomic", "pass", "auto"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * attn.h -- C ABI of libattn, exact softmax attention (forward and backward)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  For every (b, h) head independently, with Q, K, V of
+ * shape (n, d) and s_ij = scale * q_i . k_j:
+ *
+ *   forward   O = softmax(S) V,  LSE_i = ln sum_j exp(s_ij)
+ *             ("Chapter 3.1 -- The cost of attention", section 2, the scaled
+ *             dot-product formula; "Flash Attention: Revolutionizing
+ *             Transformer Efficiency", "Standard attention: a quick summary")
+ *   backward  for a scalar loss with gradient dO = dL/dO:
+ *             P = exp(S - LSE), dV = P^T dO, dP = dO V^T, D_i = dO_i . O_i,
+ *             dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q
+ *             (the pages name the backward pass and its recomputation of P --
+ *             "Chapter 3.1", section 5; "On the fine-grained I/O complexity
+ *             of attention backward passes", Methodology -- but print no
+ *             formulas; these are the exact chain-rule derivatives).
+ *   causal    optional mask: s_ij = -inf for j > i (applied before the row
+ *             maximum, so P_ij = 0 there).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are DEVICE pointers to contiguous row-major [B][H][n][d]
+ *     arrays (d innermost).  LSE and D are fp32 [B][H][n], natural log.
+ *     Q, K, V, O, dO, dQ, dK, dV share one element type (attn_dtype).
+ *   - Every pointer must be 16-byte aligned.  Outputs are fully
+ *     overwritten and must not alias any input.
+ *   - The caller owns every buffer.  The library never allocates device
+ *     memory, never frees, and never synchronises, except attn_status().
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously.  The return value reports argument
+ *     and launch errors only (attn_status_t, 0 = success).  Errors detected
+ *     on the device (a bounded wait that ran out) are recorded in a device
+ *     status word read by attn_status().
+ *   - bf16 path: d in {64, 128, 256}; fp32 path: 1 <= d <= 256.  Any n >= 1.
+ *   - Thread-safe: the only global state is the device status word.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/* How attn_bwd combines dQ = scale * sum_j dS_ij k_j across key tiles. */
+typedef enum {
+  ATTN_DQ_AUTO = 0,   /* the measured default for the shape */
+  ATTN_DQ_ATOMIC = 1, /* key-tile kernel adds its dQ share into an fp32
+                         workspace accumulator with atomics, then converts */
+  ATTN_DQ_PASS = 2    /* separate query-tile kernel recomputes S, dP, dS and
+                         sums dQ with no atomics */
+} attn_dq_mode;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, size < 1, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head dim not supported for this dtype/path */
+  ATTN_ERR_WORKSPACE = 3,     /* workspace null or smaller than required */
+  ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 5 /* a bounded device-side wait ran out */
+} attn_status_t;
+
+/*
+ * attn_fwd -- forward pass.
+ *   Q, K, V : inputs  [B][H][n][d]
+ *   O       : output  [B][H][n][d]
+ *   LSE     : output  fp32 [B][H][n], LSE_i = ln sum_j exp(s_ij)
+ *   scale   : finite score multiplier (usually 1/sqrt(d))
+ *   causal  : 0 or 1
+ * bf16: one fused tensor-core kernel (TMA tiles, tcgen05 MMAs with TMEM
+ * accumulators, online softmax: "Flash Attention: Revolutionizing
+ * Transformer Efficiency", "The mathematics behind Flash Attention",
+ * formulas 1-2, with the running-sum factor restored).  fp32: exact fp32
+ * SIMT kernel.
+ */
+ATTN_API int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+             int B, int H, int n, int d, attn_dtype dtype, float scale,
+             int causal, void* stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs for
+ * this shape and dQ mode (row statistics, plus the fp32 dQ accumulator in
+ * ATTN_DQ_ATOMIC mode).  Returns 0 for invalid arguments.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype,
+                               int causal, attn_dq_mode mode);
+
+/*
+ * attn_bwd -- backward pass.
+ *   Q, K, V, O, dO : inputs [B][H][n][d]; O is the forward output.
+ *   LSE            : input fp32 [B][H][n] from attn_fwd.
+ *   dQ, dK, dV     : outputs [B][H][n][d].
+ *   workspace      : device buffer of at least attn_bwd_workspace_size(...)
+ *                    bytes, 256-byte aligned, owned by the caller; contents
+ *                    on entry are ignored.
+ * Computes D = rowsum(dO o O) in a preprocessing kernel, then recomputes P
+ * from LSE tile by tile (P is never stored), accumulating dK and dV per key
+ * tile in tensor memory.
+ */
+ATTN_API int attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+             int B, int H, int n, int d, attn_dtype dtype, float scale,
+             int causal, attn_dq_mode mode, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages attn_bwd runs, exported so a caller can schedule or time
+ * them separately (same arguments and workspace as attn_bwd; call them in
+ * this order on one stream, with the same dQ mode):
+ *   attn_bwd_preprocess  D_i = dO_i . O_i and the log2-scaled LSE into the
+ *                        workspace; zeroes the fp32 dQ accumulator
+ *                        (ATTN_DQ_ATOMIC).  Bandwidth-bound.
+ *   attn_bwd_dkdv        the fused key-tile kernel: recomputes P from LSE and
+ *                        writes dK and dV; in ATTN_DQ_ATOMIC mode it also adds
+ *                        every dQ share into the workspace accumulator.
+ *   attn_bwd_dq          ATTN_DQ_ATOMIC: converts the accumulator to dQ;
+ *                        ATTN_DQ_PASS: the query-tile kernel computes dQ.
+ * Pointers not used by a stage may be NULL.
+ */
+ATTN_API int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
+             int B, int H, int n, int d, attn_dtype dtype, int causal,
+             attn_dq_mode mode, void* workspace, size_t workspace_bytes,
+             void* stream);
+ATTN_API int attn_bwd_dkdv(const void* Q, const void* K, const void* V,
+             const void* dO, void* dK, void* dV, int B, int H, int n, int d,
+             attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+             void* workspace, size_t workspace_bytes, void* stream);
+ATTN_API int attn_bwd_dq(const void* Q, const void* K, const void* V,
+             const void* dO, void* dQ, int B, int H, int n, int d,
+             attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Materialise-P comparison path (bf16 only, d in {64,128,256}).  The plainest
+ * reading of the small-cache algorithm of "On the fine-grained I/O
+ * complexity of attention backward passes" (Methodology step 3: it reads
+ * and writes the n x n attention matrices and n x d intermediates
+ * explicitly), which is also the standard attention of "Flash Attention:
+ * Revolutionizing Transformer Efficiency" ("Standard attention", the score
+ * matrix written to and read back from HBM).  Every n x n matrix goes
+ * through HBM: forward S (fp32) -> P (bf16) -> O = PV; backward
+ * dV = P^T dO, dP = dO V^T (fp32), dS (bf16), dQ = scale dS K,
+ * dK = scale dS^T Q.  Results equal attn_fwd/attn_bwd up to rounding.
+ * Workspace: attn_mat_workspace_size bytes, 256-byte aligned; the forward
+ * leaves P in the workspace and attn_mat_bwd reads it, so pass the same
+ * workspace to both without touching it in between.
+ */
+ATTN_API size_t attn_mat_workspace_size(int B, int H, int n, int d);
+ATTN_API int attn_mat_fwd(const void* Q, const void* K, const void* V, void* O,
+                 float* LSE, int B, int H, int n, int d, float scale,
+                 int causal, void* workspace, size_t workspace_bytes,
+                 void* stream);
+ATTN_API int attn_mat_bwd(const void* Q, const void* K, const void* V, const void* O,
+                 const void* dO, const float* LSE, void* dQ, void* dK,
+                 void* dV, int B, int H, int n, int d, float scale,
+                 int causal, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
+ * attn_gemm_bf16 -- batched tensor-core GEMM used by the materialise-P path,
+ * exported for testing the tcgen05/TMA building blocks in isolation:
+ *   C[b] = alpha * op(A[b]) * op(B[b]),  b in [0, batch)
+ * A[b] is M x K: row-major [M][K] if a_kmajor, else stored as [K][M].
+ * B[b] is K x N: stored [N][K] if b_kmajor, else row-major [K][N].
+ * C[b] is row-major [M][N], fp32 if c_f32 else bf16.  Batches are packed
+ * with strides M*K, K*N, M*N elements.  K must be a multiple of 8 and the
+ * contiguous dimension of every operand a multiple of 8 elements.
+ */
+ATTN_API int attn_gemm_bf16(const void* A, const void* Bm, void* C, int batch, int M,
+                   int N, int K, int a_kmajor, int b_kmajor, int c_f32,
+                   float alpha, void* stream);
+
+/* Synchronises `stream`, then returns and clears the first device-side
+ * error recorded since the last call (ATTN_OK if none). */
+ATTN_API int attn_status(void* stream);
+
+/* Static description of a status code. */
+ATTN_API const char* attn_strerror(int code);
+
+/* Library version string. */
+ATTN_API const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

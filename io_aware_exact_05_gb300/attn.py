@@ -1,0 +1,229 @@
+"""ctypes binding of libattn (include/attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libattn.so``.  Functions keep the C names and take torch tensors
+(device memory, contiguous [B, H, n, d]) plus the current CUDA stream.  If the
+library is missing, every call raises: there is no fallback implementation.
+"""
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "ATTN_BF16", "ATTN_F32", "ATTN_DQ_AUTO", "ATTN_DQ_ATOMIC", "ATTN_DQ_PASS",
+    "AttnError", "lib", "lib_path",
+    "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
+    "attn_mat_fwd", "attn_mat_bwd", "attn_mat_workspace_size",
+    "attn_gemm_bf16", "attn_status", "attn_strerror", "attn_version",
+    "forward", "backward",
+]
+
+ATTN_BF16, ATTN_F32 = 0, 1
+ATTN_DQ_AUTO, ATTN_DQ_ATOMIC, ATTN_DQ_PASS = 0, 1, 2
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def lib_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s failed: %s (code %d)" % (where, attn_strerror(code), code))
+
+
+def lib():
+    """Load libattn.so (built in-tree by __graft_entry__.build())."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "libattn.so is not built (%s); run __graft_entry__.build()" % path)
+            L = ctypes.CDLL(path)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+            L.attn_fwd.restype = i
+            L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.attn_bwd_workspace_size.restype = sz
+            L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.attn_bwd.restype = i
+            L.attn_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
+            L.attn_bwd_preprocess.restype = i
+            L.attn_bwd_dkdv.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.attn_bwd_dkdv.restype = i
+            L.attn_bwd_dq.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.attn_bwd_dq.restype = i
+            L.attn_mat_workspace_size.argtypes = [i, i, i, i]
+            L.attn_mat_workspace_size.restype = sz
+            L.attn_mat_fwd.argtypes = [vp] * 5 + [i, i, i, i, f, i, vp, sz, vp]
+            L.attn_mat_fwd.restype = i
+            L.attn_mat_bwd.argtypes = [vp] * 9 + [i, i, i, i, f, i, vp, sz, vp]
+            L.attn_mat_bwd.restype = i
+            L.attn_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            L.attn_gemm_bf16.restype = i
+            L.attn_status.argtypes = [vp]
+            L.attn_status.restype = i
+            L.attn_strerror.argtypes = [i]
+            L.attn_strerror.restype = ctypes.c_char_p
+            L.attn_version.argtypes = []
+            L.attn_version.restype = ctypes.c_char_p
+            _LIB = L
+    return _LIB
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, n, d], got %s" % (tuple(q.shape),))
+    return tuple(int(x) for x in q.shape)
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise AttnError(rc, where)
+
+
+def attn_strerror(code):
+    return lib().attn_strerror(int(code)).decode()
+
+
+def attn_version():
+    return lib().attn_version().decode()
+
+
+def attn_status(stream=None):
+    """Synchronise the stream; return and clear the first device-side error."""
+    return lib().attn_status(_stream(stream))
+
+
+def attn_fwd(Q, K, V, O, LSE, scale, causal, stream=None):
+    B, H, n, d = _shape(Q)
+    rc = lib().attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, n, d,
+                        _dtype_code(Q), float(scale), int(bool(causal)), _stream(stream))
+    _check(rc, "attn_fwd")
+
+
+def attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode=ATTN_DQ_AUTO):
+    return int(lib().attn_bwd_workspace_size(B, H, n, d, dtype, int(bool(causal)), int(mode)))
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AUTO,
+             workspace=None, stream=None):
+    B, H, n, d = _shape(Q)
+    dt = _dtype_code(Q)
+    need = attn_bwd_workspace_size(B, H, n, d, dt, causal, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    rc = lib().attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                        _ptr(dK), _ptr(dV), B, H, n, d, dt, float(scale),
+                        int(bool(causal)), int(mode), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_bwd")
+
+
+def _ws(workspace):
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def attn_bwd_preprocess(O, dO, LSE, causal, mode, workspace, stream=None):
+    B, H, n, d = _shape(O)
+    wp, wb = _ws(workspace)
+    rc = lib().attn_bwd_preprocess(_ptr(O), _ptr(dO), _ptr(LSE), B, H, n, d, _dtype_code(O),
+                                   int(bool(causal)), int(mode), wp, wb, _stream(stream))
+    _check(rc, "attn_bwd_preprocess")
+
+
+def attn_bwd_dkdv(Q, K, V, dO, dK, dV, scale, causal, mode, workspace, stream=None):
+    B, H, n, d = _shape(Q)
+    wp, wb = _ws(workspace)
+    rc = lib().attn_bwd_dkdv(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dK), _ptr(dV), B, H, n, d,
+                             _dtype_code(Q), float(scale), int(bool(causal)), int(mode), wp, wb,
+                             _stream(stream))
+    _check(rc, "attn_bwd_dkdv")
+
+
+def attn_bwd_dq(Q, K, V, dO, dQ, scale, causal, mode, workspace, stream=None):
+    B, H, n, d = _shape(dQ)
+    wp, wb = _ws(workspace)
+    rc = lib().attn_bwd_dq(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), B, H, n, d,
+                           _dtype_code(dQ), float(scale), int(bool(causal)), int(mode), wp, wb,
+                           _stream(stream))
+    _check(rc, "attn_bwd_dq")
+
+
+def attn_mat_workspace_size(B, H, n, d):
+    return int(lib().attn_mat_workspace_size(B, H, n, d))
+
+
+def attn_mat_fwd(Q, K, V, O, LSE, scale, causal, workspace, stream=None):
+    B, H, n, d = _shape(Q)
+    rc = lib().attn_mat_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, n, d,
+                            float(scale), int(bool(causal)), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_mat_fwd")
+
+
+def attn_mat_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, workspace, stream=None):
+    B, H, n, d = _shape(Q)
+    rc = lib().attn_mat_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
+                            _ptr(dQ), _ptr(dK), _ptr(dV), B, H, n, d, float(scale),
+                            int(bool(causal)), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_mat_bwd")
+
+
+def attn_gemm_bf16(A, Bm, C, batch, M, N, K, a_kmajor, b_kmajor, alpha=1.0, stream=None):
+    c_f32 = C.dtype == torch.float32
+    rc = lib().attn_gemm_bf16(_ptr(A), _ptr(Bm), _ptr(C), batch, M, N, K, int(bool(a_kmajor)),
+                              int(bool(b_kmajor)), int(c_f32), float(alpha), _stream(stream))
+    _check(rc, "attn_gemm_bf16")
+
+
+# ---------------------------------------------------------------- conveniences
+
+def forward(q, k, v, causal=False, scale=None, stream=None):
+    """Allocate O and LSE with torch and run attn_fwd.  Returns (O, LSE)."""
+    B, H, n, d = _shape(q)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, do, lse, causal=False, scale=None, mode=ATTN_DQ_AUTO,
+             workspace=None, stream=None):
+    """Allocate dQ, dK, dV with torch and run attn_bwd.  Returns (dQ, dK, dV)."""
+    d = q.shape[-1]
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)
+    return dq, dk, dv

@@ -1,0 +1,340 @@
+// attn_api.cu -- the extern "C" entry points of libattn (declared in
+// include/attn.h): argument checks, workspace carving and kernel dispatch.
+#include <cmath>
+#include <cstdint>
+#include <initializer_list>
+
+#include "kernels.h"
+
+namespace attn {
+int read_and_clear_status(cudaStream_t st);
+}
+
+using namespace attn;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int n, int d, float scale, int causal) {
+  if (B < 1 || H < 1 || n < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;   // heads map to grid.y
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+bool bf16_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+// dQ mode actually used for a bf16 shape.  The key-tile kernel can carry the
+// dQ accumulator in tensor memory only for d <= 128; d = 256 always uses the
+// separate query-tile pass.
+attn_dq_mode resolve_mode(int d, attn_dq_mode mode) {
+  if (mode == ATTN_DQ_AUTO) return d <= 128 ? ATTN_DQ_ATOMIC : ATTN_DQ_PASS;
+  return mode;
+}
+
+struct BwdWorkspace {
+  float* lse2;
+  float* delta;
+  float* dq_acc;
+  size_t bytes;
+};
+
+BwdWorkspace carve_bwd(void* base, int BH, int n, int d, attn_dtype dtype, attn_dq_mode mode) {
+  BwdWorkspace w{};
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  if (dtype == ATTN_F32) {
+    w.delta = reinterpret_cast<float*>(p);
+    off = round_up((size_t)BH * n * 4, kAlign);
+  } else {
+    const size_t n_pad = round_up(n, 128);
+    w.lse2 = reinterpret_cast<float*>(p + off);
+    off += round_up((size_t)BH * n_pad * 4, kAlign);
+    w.delta = reinterpret_cast<float*>(p + off);
+    off += round_up((size_t)BH * n_pad * 4, kAlign);
+    if (mode == ATTN_DQ_ATOMIC) {
+      w.dq_acc = reinterpret_cast<float*>(p + off);
+      off += round_up((size_t)BH * n * d * 4, kAlign);
+    }
+  }
+  w.bytes = off;
+  return w;
+}
+
+struct MatWorkspace {
+  float* s;        // S, later dP: fp32 [BH][n][n]
+  void* p;         // P, later dS: bf16 [BH][n][n]
+  float* delta;    // [BH][n]
+  float* lse2;     // [BH][n]
+  size_t bytes;
+};
+
+MatWorkspace carve_mat(void* base, int BH, int n) {
+  MatWorkspace w{};
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t nn = (size_t)BH * n * n;
+  size_t off = 0;
+  w.s = reinterpret_cast<float*>(p + off);
+  off += round_up(nn * 4, kAlign);
+  w.p = p + off;
+  off += round_up(nn * 2, kAlign);
+  w.delta = reinterpret_cast<float*>(p + off);
+  off += round_up((size_t)BH * n * 4, kAlign);
+  w.lse2 = reinterpret_cast<float*>(p + off);
+  off += round_up((size_t)BH * n * 4, kAlign);
+  w.bytes = off;
+  return w;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+             int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return ATTN_ERR_INVALID_ARG;
+  int rc = check_common(B, H, n, d, scale, causal);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  if (dtype == ATTN_F32) {
+    if (d > 256) return ATTN_ERR_UNSUPPORTED;
+    return cuda_rc(launch_fwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                  static_cast<const float*>(V), static_cast<float*>(O), LSE, BH, n,
+                                  d, scale, causal, st));
+  }
+  if (dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
+  return launch_fwd_tc(Q, K, V, O, LSE, BH, n, d, scale, causal, default_ctl(), st);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int causal,
+                               attn_dq_mode mode) {
+  if (check_common(B, H, n, d, 1.0f, causal) != ATTN_OK) return 0;
+  if (dtype == ATTN_F32) {
+    if (d > 256) return 0;
+    return carve_bwd(nullptr, B * H, n, d, dtype, mode).bytes;
+  }
+  if (dtype != ATTN_BF16 || !bf16_head_dim(d)) return 0;
+  const attn_dq_mode m = resolve_mode(d, mode);
+  if (m == ATTN_DQ_ATOMIC && d > 128) return 0;
+  return carve_bwd(nullptr, B * H, n, d, dtype, m).bytes;
+}
+
+// Shared checks of the backward stages.  On success fills the resolved mode
+// and the carved workspace.
+static int bwd_setup(int B, int H, int n, int d, attn_dtype dtype, float scale, int causal,
+                     attn_dq_mode mode, void* workspace, size_t workspace_bytes,
+                     attn_dq_mode* resolved, BwdWorkspace* w) {
+  int rc = check_common(B, H, n, d, scale, causal);
+  if (rc) return rc;
+  if (mode != ATTN_DQ_AUTO && mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_PASS)
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype == ATTN_F32) {
+    if (d > 256) return ATTN_ERR_UNSUPPORTED;
+    *resolved = mode;
+  } else if (dtype == ATTN_BF16) {
+    if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
+    *resolved = resolve_mode(d, mode);
+    if (*resolved == ATTN_DQ_ATOMIC && d > 128) return ATTN_ERR_UNSUPPORTED;
+  } else {
+    return ATTN_ERR_INVALID_ARG;
+  }
+  *w = carve_bwd(workspace, B * H, n, d, dtype, *resolved);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) || workspace_bytes < w->bytes)
+    return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+static bool ptrs_ok(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return false;
+  return true;
+}
+
+int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, int H, int n,
+                        int d, attn_dtype dtype, int causal, attn_dq_mode mode, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!ptrs_ok({O, dO, LSE})) return ATTN_ERR_INVALID_ARG;
+  attn_dq_mode m;
+  BwdWorkspace w;
+  int rc = bwd_setup(B, H, n, d, dtype, 1.0f, causal, mode, workspace, workspace_bytes, &m, &w);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32)
+    return cuda_rc(launch_delta_f32(static_cast<const float*>(O), static_cast<const float*>(dO),
+                                    w.delta, B * H, n, d, st));
+  return cuda_rc(launch_delta_bf16(O, dO, LSE, w.delta, w.lse2,
+                                   m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr, B * H, n,
+                                   (int)round_up(n, 128), d, st));
+}
+
+int attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                  int B, int H, int n, int d, attn_dtype dtype, float scale, int causal,
+                  attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ptrs_ok({Q, K, V, dO, dK, dV})) return ATTN_ERR_INVALID_ARG;
+  attn_dq_mode m;
+  BwdWorkspace w;
+  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32)
+    return ATTN_ERR_INVALID_ARG;   // the fp32 dK/dV kernel needs LSE: use attn_bwd
+  return launch_bwd_kv_tc(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr,
+                          dK, dV, B * H, n, (int)round_up(n, 128), d, scale, causal, default_ctl(),
+                          st);
+}
+
+int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
+                int H, int n, int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ptrs_ok({dQ})) return ATTN_ERR_INVALID_ARG;
+  attn_dq_mode m;
+  BwdWorkspace w;
+  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;   // use attn_bwd
+  if (m == ATTN_DQ_ATOMIC) return cuda_rc(launch_dq_convert(w.dq_acc, dQ, (size_t)B * H * n * d, st));
+  if (!ptrs_ok({Q, K, V, dO})) return ATTN_ERR_INVALID_ARG;
+  return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, n, (int)round_up(n, 128), d,
+                         scale, causal, default_ctl(), st);
+}
+
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
+             attn_dtype dtype, float scale, int causal, attn_dq_mode mode, void* workspace,
+             size_t workspace_bytes, void* stream) {
+  if (!ptrs_ok({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID_ARG;
+  attn_dq_mode m;
+  BwdWorkspace w;
+  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  if (dtype == ATTN_F32) {
+    const float *q = static_cast<const float*>(Q), *k = static_cast<const float*>(K),
+                *v = static_cast<const float*>(V), *g = static_cast<const float*>(dO);
+    rc = cuda_rc(launch_delta_f32(static_cast<const float*>(O), g, w.delta, BH, n, d, st));
+    if (rc) return rc;
+    rc = cuda_rc(launch_bwd_dkdv_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dK),
+                                     static_cast<float*>(dV), BH, n, d, scale, causal, st));
+    if (rc) return rc;
+    return cuda_rc(launch_bwd_dq_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dQ), BH, n, d,
+                                     scale, causal, st));
+  }
+  rc = attn_bwd_preprocess(O, dO, LSE, B, H, n, d, dtype, causal, mode, workspace,
+                           workspace_bytes, stream);
+  if (rc) return rc;
+  rc = attn_bwd_dkdv(Q, K, V, dO, dK, dV, B, H, n, d, dtype, scale, causal, mode, workspace,
+                     workspace_bytes, stream);
+  if (rc) return rc;
+  return attn_bwd_dq(Q, K, V, dO, dQ, B, H, n, d, dtype, scale, causal, mode, workspace,
+                     workspace_bytes, stream);
+}
+
+size_t attn_mat_workspace_size(int B, int H, int n, int d) {
+  if (check_common(B, H, n, d, 1.0f, 0) != ATTN_OK) return 0;
+  if (!bf16_head_dim(d) || (n % 8) != 0) return 0;
+  return carve_mat(nullptr, B * H, n).bytes;
+}
+
+int attn_mat_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int n, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  const void* ptrs[] = {Q, K, V, O, LSE};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  int rc = check_common(B, H, n, d, scale, causal);
+  if (rc) return rc;
+  if (!bf16_head_dim(d) || (n % 8) != 0) return ATTN_ERR_UNSUPPORTED;
+  const int BH = B * H;
+  MatWorkspace w = carve_mat(workspace, BH, n);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) || workspace_bytes < w.bytes)
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const KernelCtl ctl = default_ctl();
+  // S = scale * Q K^T            (A = Q K-major, B = K stored [n][d]: K-major)
+  rc = launch_gemm_bf16(Q, K, w.s, BH, n, n, d, true, true, true, scale, ctl, st);
+  if (rc) return rc;
+  // P = softmax(S), LSE
+  rc = cuda_rc(launch_mat_softmax(w.s, w.p, LSE, BH, n, scale, causal, st));
+  if (rc) return rc;
+  // O = P V                      (A = P K-major, B = V stored [K=n][N=d]: MN-major)
+  return launch_gemm_bf16(w.p, V, O, BH, n, d, n, true, false, false, 1.0f, ctl, st);
+}
+
+int attn_mat_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  int rc = check_common(B, H, n, d, scale, causal);
+  if (rc) return rc;
+  if (!bf16_head_dim(d) || (n % 8) != 0) return ATTN_ERR_UNSUPPORTED;
+  const int BH = B * H;
+  MatWorkspace w = carve_mat(workspace, BH, n);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) || workspace_bytes < w.bytes)
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const KernelCtl ctl = default_ctl();
+  // dV = P^T dO                  (A = P^T: P stored [K=q][M=k], MN-major; B = dO MN-major)
+  rc = launch_gemm_bf16(w.p, dO, dV, BH, n, d, n, false, false, false, 1.0f, ctl, st);
+  if (rc) return rc;
+  // dP = dO V^T                  (A = dO K-major, B = V stored [N=k][K=d]: K-major)
+  rc = launch_gemm_bf16(dO, V, w.s, BH, n, n, d, true, true, true, 1.0f, ctl, st);
+  if (rc) return rc;
+  // D = rowsum(dO o O)
+  rc = cuda_rc(launch_delta_bf16(O, dO, LSE, w.delta, w.lse2, nullptr, BH, n, n, d, st));
+  if (rc) return rc;
+  // dS = P o (dP - D), written over P
+  rc = cuda_rc(launch_mat_dsoftmax(w.p, w.s, w.delta, w.p, BH, n, st));
+  if (rc) return rc;
+  // dQ = scale dS K              (A = dS K-major, B = K stored [K=k][N=d]: MN-major)
+  rc = launch_gemm_bf16(w.p, K, dQ, BH, n, d, n, true, false, false, scale, ctl, st);
+  if (rc) return rc;
+  // dK = scale dS^T Q            (A = dS^T: MN-major, B = Q stored [K=q][N=d]: MN-major)
+  return launch_gemm_bf16(w.p, Q, dK, BH, n, d, n, false, false, false, scale, ctl, st);
+}
+
+int attn_gemm_bf16(const void* A, const void* Bm, void* C, int batch, int M, int N, int K,
+                   int a_kmajor, int b_kmajor, int c_f32, float alpha, void* stream) {
+  if (!A || !Bm || !C || !aligned16(A) || !aligned16(Bm) || !aligned16(C))
+    return ATTN_ERR_INVALID_ARG;
+  if (batch < 1 || M < 1 || N < 1 || K < 1 || batch > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return ATTN_ERR_INVALID_ARG;
+  if (K % 8) return ATTN_ERR_UNSUPPORTED;
+  if (!a_kmajor && (M % 8)) return ATTN_ERR_UNSUPPORTED;
+  if (!b_kmajor && (N % 8)) return ATTN_ERR_UNSUPPORTED;
+  return launch_gemm_bf16(A, Bm, C, batch, M, N, K, a_kmajor != 0, b_kmajor != 0, c_f32 != 0,
+                          alpha, default_ctl(), static_cast<cudaStream_t>(stream));
+}
+
+int attn_status(void* stream) { return read_and_clear_status(static_cast<cudaStream_t>(stream)); }
+
+const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, size, scale)";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or head dimension for this path";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a device-side barrier wait ran out of time";
+    default: return "unknown status code";
+  }
+}
+
+const char* attn_version(void) { return "libattn 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,680 @@
+// bwd_tc.cu -- fused exact attention backward on the tcgen05 tensor cores.
+//
+// The backward pass never stores P: it recomputes it tile by tile from the
+// saved logsumexp ("Chapter 3.1 -- The cost of attention", section 5;
+// "Flash Attention: Revolutionizing Transformer Efficiency", key idea 2,
+// recomputation), with P_ij = 2^(s_ij * scale * log2e - LSE2_i) and
+// LSE2 = LSE * log2e, and the exact chain rule
+//   dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
+//   dK = scale dS^T Q,   D_i = dO_i . O_i (from the preprocessing kernel).
+//
+// bwd_kv_kernel -- one CTA per 128-key tile of one head.  Everything is
+// computed transposed so the key index lands on the TMEM lanes:
+//   S^T  = K Q_i^T     (SS-MMA, M = 128 keys, N = BM queries)
+//   dP^T = V dO_i^T    (SS-MMA)
+//   P^T  = 2^(S^T * c - LSE2)       -> bf16 back into TMEM (over S^T)
+//   dV  += P^T dO_i    (TS-MMA: A = P^T from TMEM, B = dO_i MN-major)
+//   dS^T = P^T o (dP^T - D)         -> bf16 into TMEM (over dP^T) and smem
+//   dK  += dS^T Q_i    (TS-MMA)
+//   dQ_i = dS K        (SS-MMA, A = dS MN-major in smem) -> TMEM, then the
+//                      dQ warpgroup adds scale * dQ_i into an fp32
+//                      accumulator in global memory with vector atomics.
+// For d = 256 the two accumulators already fill the 512 TMEM columns, so
+// the kernel runs twice per key tile (grid.z = 2), each producing one
+// 128-wide half of dK and dV, and dQ comes from bwd_q_kernel.
+//
+// bwd_q_kernel -- one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T,
+// dS = P o (dP - D) -> bf16 TMEM, dQ += dS K_j (TS-MMA); no atomics.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// ============================================================================ key-tile kernel
+template <int D, bool DQ>
+struct KvCfg {
+  static constexpr int BNK = 128;                    // keys per CTA (TMEM lanes)
+  static constexpr int BM = (D == 256) ? 64 : 128;   // queries per iteration
+  static constexpr int DO = (D == 256) ? 128 : D;    // dK/dV columns per CTA
+  static constexpr int STG = (D == 256) ? 1 : 2;
+  static constexpr bool WITH_DQ = DQ;                // atomic dQ shares from this kernel
+  static constexpr bool DS_ALIAS = DQ && D == 128;   // dS reuses the dO stage buffer
+  static constexpr int NKB = D / 64;
+  static constexpr uint32_t KV_BYTES = BNK * D * 2;
+  static constexpr uint32_t QT_BYTES = BM * D * 2;   // one Q or dO tile
+  static constexpr uint32_t STAT_BYTES = BM * 4;     // LSE2 or D of the tile
+  static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024;   // Q, dO, LSE2 + D (padded)
+  static constexpr uint32_t K_OFF = 0;
+  static constexpr uint32_t V_OFF = KV_BYTES;
+  static constexpr uint32_t ST_OFF = 2 * KV_BYTES;
+  static constexpr uint32_t DS_OFF = ST_OFF + STG * STAGE;  // dedicated dS buffer (D = 64)
+  static constexpr uint32_t DS_BYTES = (WITH_DQ && !DS_ALIAS) ? BM * BNK * 2 : 0;
+  static constexpr uint32_t BAR_OFF = DS_OFF + DS_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  // TMEM columns
+  static constexpr int DV_COL = 0;
+  static constexpr int DK_COL = DO;
+  static constexpr int S_COL = 2 * DO;
+  static constexpr int DP_COL = 2 * DO + BM;
+  static constexpr int NTHREADS = WITH_DQ ? 512 : 384;
+  static_assert(2 * DO + 2 * BM <= 512, "tensor memory budget");
+  static_assert(!WITH_DQ || (BM == 128 && D <= BM), "dQ tile reuses the S columns");
+  static_assert(!(D == 256 && DQ), "d = 256 takes dQ from the query-tile kernel");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8, K_DVD = 9,
+             K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13 };
+
+template <int D, bool DQ>
+__global__ void __launch_bounds__(KvCfg<D, DQ>::NTHREADS, 1)
+bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const float* __restrict__ LSE2, const float* __restrict__ Dv,
+              float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
+              __nv_bfloat16* __restrict__ dV, int n, int n_pad, float scale, float scale_log2,
+              int causal, KernelCtl ctl) {
+  using C = KvCfg<D, DQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1k(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + C::BAR_OFF;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, bh = blockIdx.y, oh = blockIdx.z;   // oh: dK/dV column half (d=256)
+  const int k0 = kt * C::BNK;
+  const int nq = (n + C::BM - 1) / C::BM;
+  const int i_start = causal ? (k0 / C::BM) : 0;
+  const int cnt = nq - i_start;   // query tiles this CTA visits (>= 1)
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(K_KV), 1);
+    for (int s = 0; s < C::STG; ++s) {
+      mbar_init(bar(K_QF + s), 1);
+      mbar_init(bar(K_QE + s), 1);
+    }
+    mbar_init(bar(K_SF), 1);
+    mbar_init(bar(K_DPF), 1);
+    mbar_init(bar(K_PR), 256);
+    mbar_init(bar(K_DSR), 256);
+    mbar_init(bar(K_DVD), 1);
+    mbar_init(bar(K_DQF), 1);
+    mbar_init(bar(K_DQE), 128);
+    mbar_init(bar(K_ACC), 1);
+    mbar_init(bar(K_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 2) tmem_alloc<512>(smem_u32(tmem_slot));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      mbar_expect_tx(bar(K_KV), 2 * C::KV_BYTES);
+#pragma unroll
+      for (int kb = 0; kb < C::NKB; ++kb) {
+        tma_load_3d(sb + C::K_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
+        tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
+      }
+      int issued_last[2] = {-1, -1};
+      for (int u = 0; u < cnt; ++u) {
+        const int s = u % C::STG;
+        const int q0 = (i_start + u) * C::BM;
+        if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+          break;
+        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
+        mbar_expect_tx(bar(K_QF + s), 2 * C::QT_BYTES + 2 * C::STAT_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb) {
+          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(K_QF + s));
+          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(K_QF + s));
+        }
+        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bh * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
+        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bh * n_pad + q0, C::STAT_BYTES,
+                  bar(K_QF + s));
+        issued_last[s] = u;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        mbar_wait(bar(K_KV), 0, &no_abort, ctl, SITE_BWD_KV);
+        for (int s = 0; s < C::STG; ++s)
+          if (issued_last[s] >= 0)
+            mbar_wait(bar(K_QF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V K-major, Q/dO K-major
+      constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS MN-major, K MN-major
+      bool ok = mbar_wait(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
+      for (int u = 0; ok && u < cnt; ++u) {
+        const int s = u % C::STG;
+        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
+        const uint32_t qa = st, ga = st + C::QT_BYTES;
+        if (!(ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
+        if (C::WITH_DQ && u > 0) {
+          if (!(ok = mbar_wait(bar(K_DQE), (u - 1) & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
+        }
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T  (contraction over d, 16 per instruction)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::S_COL, sdesc_sw128(ka + koff, 16, 1024), sdesc_sw128(qa + qoff, 16, 1024),
+                 id_s, kk > 0);
+        }
+        tc_commit(bar(K_SF));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t voff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
+          const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::DP_COL, sdesc_sw128(va + voff, 16, 1024), sdesc_sw128(ga + goff, 16, 1024),
+                 id_s, kk > 0);
+        }
+        tc_commit(bar(K_DPF));
+        // dV += P^T dO   (contraction over the BM queries of this tile)
+        if (!(ok = mbar_wait(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
+        tc_fence_after();
+        const uint32_t boff = oh * 2 * (C::BM * 128);   // first dO/Q column box of this half
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk) {
+          // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
+          const int h = (16 * kk) / (C::BM / 2);
+          const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
+                 sdesc_sw128(ga + boff + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+        }
+        if (C::DS_ALIAS) tc_commit(bar(K_DVD));
+        // dK += dS^T Q ; dQ_i = dS K
+        if (!(ok = mbar_wait(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk) {
+          const int h = (16 * kk) / (C::BM / 2);
+          const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
+          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + acol,
+                 sdesc_sw128(qa + boff + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+        }
+        if (C::WITH_DQ) {
+          const uint32_t dsa = C::DS_ALIAS ? ga : (sb + C::DS_OFF);
+#pragma unroll
+          for (int kk = 0; kk < C::BNK / 16; ++kk)
+            mma_ss(tmem + C::S_COL, sdesc_sw128(dsa + kk * 2048, C::BNK * 128, 1024),
+                   sdesc_sw128(ka + kk * 2048, C::BNK * 128, 1024), id_dq, kk > 0);
+          tc_commit(bar(K_DQF));
+        }
+        tc_commit(bar(K_QE + s));
+      }
+      tc_commit(bar(K_ACC));
+      if (*abort_flag) {
+        tc_commit(bar(K_DRAIN));
+        volatile int no_abort = 0;
+        mbar_wait(bar(K_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- compute
+    const int q = warp & 3, h = (warp - 4) >> 2;
+    const int r = q * 32 + lane;          // key row within the tile (TMEM lane)
+    const int key = k0 + r;
+    constexpr int NC = C::BM / 2;         // query columns of this thread
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
+    const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
+    bool ok = true;
+    for (int u = 0; u < cnt; ++u) {
+      const int s = u % C::STG;
+      const int q0 = (i_start + u) * C::BM;
+      const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
+      const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
+      const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
+      ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+      ok = ok && mbar_wait(bar(K_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const bool masked = causal && (k0 + C::BNK - 1 > q0);
+      const int qbase = q0 + h * NC;     // first query column of this thread
+      float p[NC];
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(s_addr + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
+          if (masked && key > qbase + c0 + i) v = 0.f;
+          p[c0 + i] = v;
+        }
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
+        tmem_st16(s_addr + c0 / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(K_PR));
+      ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t ds[NC / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(dp_addr + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]);
+          const float b = p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]);
+          ds[c0 / 2 + i] = pack_bf16x2(a, b);
+        }
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < NC / 2; c0 += 16) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = ds[c0 + i];
+        tmem_st16(dp_addr + c0, pk);
+      }
+      tmem_st_wait();
+      if (C::WITH_DQ) {
+        if (C::DS_ALIAS) {
+          ok = mbar_wait(bar(K_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        // dS as the MN-major A operand of dQ = dS K: query block h (64 queries)
+        // is one 128-byte row per key, eight 16-byte chunks, 128-byte swizzle.
+        uint8_t* dsb = C::DS_ALIAS ? const_cast<uint8_t*>(stp) + C::QT_BYTES : smem + C::DS_OFF;
+        uint8_t* rowp = dsb + h * (C::BNK * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
+              make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(K_DSR));
+    }
+    // ---- epilogue: half 0 writes dV, half 1 writes dK (scaled)
+    if (ok) {
+      ok = mbar_wait(bar(K_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const uint32_t src = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
+      __nv_bfloat16* dst = (h == 0 ? dV : dK) + ((size_t)bh * n + key) * D + oh * C::DO;
+      const float mul = h == 0 ? 1.f : scale;
+#pragma unroll 1
+      for (int c0 = 0; c0 < C::DO; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(src + c0, rr);
+        tmem_ld_wait();
+        if (key < n) store32_bf16(dst + c0, rr, mul);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;     // query row within the tile
+    const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::S_COL;
+    for (int u = 0; u < cnt; ++u) {
+      bool ok = mbar_wait(bar(K_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int qrow = (i_start + u) * C::BM + r;
+      float* dst = dQacc + ((size_t)bh * n + qrow) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        uint32_t a[32], b[32];
+        tmem_ld32(src + c0, a);
+        tmem_ld32(src + c0 + 32, b);
+        tmem_ld_wait();
+        if (c0 + 64 >= D) {   // all of dQ_i is in registers: release the columns
+          tc_fence_before();
+          mbar_arrive(bar(K_DQE));
+        }
+        if (qrow < n) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4(dst + c0 + i, scale * __uint_as_float(a[i]), scale * __uint_as_float(a[i + 1]),
+                       scale * __uint_as_float(a[i + 2]), scale * __uint_as_float(a[i + 3]));
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4(dst + c0 + 32 + i, scale * __uint_as_float(b[i]),
+                       scale * __uint_as_float(b[i + 1]), scale * __uint_as_float(b[i + 2]),
+                       scale * __uint_as_float(b[i + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc<512>(tmem);
+}
+
+// ============================================================================ query-tile kernel
+template <int D>
+struct QCfg {
+  static constexpr int BM = 128;                     // queries per CTA (TMEM lanes)
+  static constexpr int BN = (D == 256) ? 64 : 128;   // keys per iteration
+  static constexpr int STG = (D == 256) ? 1 : 2;
+  static constexpr int NKB = D / 64;
+  static constexpr uint32_t QT_BYTES = BM * D * 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t G_OFF = QT_BYTES;
+  static constexpr uint32_t ST_OFF = 2 * QT_BYTES;   // stages of (K_j, V_j)
+  static constexpr uint32_t BAR_OFF = ST_OFF + STG * 2 * KV_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int S_COL = 0;
+  static constexpr int DP_COL = BN;
+  static constexpr int DQ_COL = 2 * BN;
+  static constexpr int NTHREADS = 384;
+  static_assert(2 * BN + D <= 512, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+enum : int { Q_QF = 0, Q_KF = 1, Q_KE = 3, Q_SF = 5, Q_DPF = 6, Q_DSR = 7, Q_ACC = 8, Q_DRAIN = 9 };
+
+template <int D>
+__global__ void __launch_bounds__(QCfg<D>::NTHREADS, 1)
+bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+             const float* __restrict__ LSE2, const float* __restrict__ Dv,
+             __nv_bfloat16* __restrict__ dQ, int n, int n_pad, float scale, float scale_log2,
+             int causal, KernelCtl ctl) {
+  using C = QCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1k(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + C::BAR_OFF;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntile = gridDim.x;
+  const int it = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int bh = blockIdx.y;
+  const int q0 = it * C::BM;
+  const int nkv = (n + C::BN - 1) / C::BN;
+  const int jend = causal ? min(nkv - 1, (q0 + C::BM - 1) / C::BN) : nkv - 1;
+  const int cnt = jend + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Q_QF), 1);
+    for (int s = 0; s < C::STG; ++s) {
+      mbar_init(bar(Q_KF + s), 1);
+      mbar_init(bar(Q_KE + s), 1);
+    }
+    mbar_init(bar(Q_SF), 1);
+    mbar_init(bar(Q_DPF), 1);
+    mbar_init(bar(Q_DSR), 256);
+    mbar_init(bar(Q_ACC), 1);
+    mbar_init(bar(Q_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 2) tmem_alloc<512>(smem_u32(tmem_slot));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      mbar_expect_tx(bar(Q_QF), 2 * C::QT_BYTES);
+#pragma unroll
+      for (int kb = 0; kb < C::NKB; ++kb) {
+        tma_load_3d(sb + C::Q_OFF + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(Q_QF));
+        tma_load_3d(sb + C::G_OFF + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(Q_QF));
+      }
+      int issued_last[2] = {-1, -1};
+      for (int j = 0; j < cnt; ++j) {
+        const int s = j % C::STG;
+        if (!mbar_wait(bar(Q_KE + s), ((j / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+          break;
+        const uint32_t st = sb + C::ST_OFF + s * 2 * C::KV_BYTES;
+        mbar_expect_tx(bar(Q_KF + s), 2 * C::KV_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb) {
+          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, j * C::BN, bh, bar(Q_KF + s));
+          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, j * C::BN, bh,
+                      bar(Q_KF + s));
+        }
+        issued_last[s] = j;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        mbar_wait(bar(Q_QF), 0, &no_abort, ctl, SITE_BWD_Q_FULL);
+        for (int s = 0; s < C::STG; ++s)
+          if (issued_last[s] >= 0)
+            mbar_wait(bar(Q_KF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_KV);
+      }
+    } else if (warp == 1 && lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);
+      constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);
+      bool ok = mbar_wait(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
+      const uint32_t qa = sb + C::Q_OFF, ga = sb + C::G_OFF;
+      for (int j = 0; ok && j < cnt; ++j) {
+        const int s = j % C::STG;
+        const uint32_t ka = sb + C::ST_OFF + s * 2 * C::KV_BYTES, va = ka + C::KV_BYTES;
+        if (!(ok = mbar_wait(bar(Q_KF + s), (j / C::STG) & 1, abort_flag, ctl, SITE_BWD_KV))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::S_COL, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
+                 id_s, kk > 0);
+        }
+        tc_commit(bar(Q_SF));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+          const uint32_t voff = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::DP_COL, sdesc_sw128(ga + goff, 16, 1024), sdesc_sw128(va + voff, 16, 1024),
+                 id_s, kk > 0);
+        }
+        tc_commit(bar(Q_DPF));
+        if (!(ok = mbar_wait(bar(Q_DSR), j & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const int h = (16 * kk) / (C::BN / 2);
+          const uint32_t acol = h * (C::BN / 2) + ((16 * kk - h * (C::BN / 2)) >> 1);
+          mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + acol,
+                 sdesc_sw128(ka + kk * 2048, C::BN * 128, 1024), id_dq, (j > 0 || kk > 0));
+        }
+        tc_commit(bar(Q_KE + s));
+      }
+      tc_commit(bar(Q_ACC));
+      if (*abort_flag) {
+        tc_commit(bar(Q_DRAIN));
+        volatile int no_abort = 0;
+        mbar_wait(bar(Q_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+      }
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, h = (warp - 4) >> 2;
+    const int r = q * 32 + lane;       // query row (TMEM lane)
+    const int qrow = q0 + r;
+    constexpr int NC = C::BN / 2;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
+    const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
+    const float lse2 = LSE2[(size_t)bh * n_pad + qrow];   // +inf on padded rows -> P = 0
+    const float dd = Dv[(size_t)bh * n_pad + qrow];
+    bool ok = true;
+    for (int j = 0; j < cnt; ++j) {
+      ok = mbar_wait(bar(Q_SF), j & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int kbase = j * C::BN + h * NC;
+      const bool masked = causal && (j * C::BN + C::BN - 1 > q0);
+      float p[NC];
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(s_addr + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2));
+          if (masked && kbase + c0 + i > qrow) v = 0.f;
+          p[c0 + i] = v;
+        }
+      }
+      ok = mbar_wait(bar(Q_DPF), j & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
+        uint32_t rr[32], pk[16];
+        tmem_ld32(dp_addr + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd),
+                              p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd));
+        tmem_st16(s_addr + c0 / 2, pk);   // dS over this half's own S columns
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Q_DSR));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(Q_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const uint32_t src = tmem + lane_off + C::DQ_COL + h * (D / 2);
+      __nv_bfloat16* dst = dQ + ((size_t)bh * n + qrow) * D + h * (D / 2);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(src + c0, rr);
+        tmem_ld_wait();
+        if (qrow < n) store32_bf16(dst + c0, rr, scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc<512>(tmem);
+}
+
+template <int D, bool DQ>
+int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
+              const float* Dv, float* dQacc, void* dK, void* dV, int BH, int n, int n_pad,
+              float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+  using C = KvCfg<D, DQ>;
+  CUtensorMap tq, tk, tv, tg;
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, C::BNK) ||
+      !make_tmap_bf16(&tv, V, D, n, BH, 64, C::BNK) || !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
+    return ATTN_ERR_CUDA;
+  auto kern = bwd_kv_kernel<D, DQ>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  dim3 grid(ceil_div(n, C::BNK), BH, D / C::DO);
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
+                                           static_cast<__nv_bfloat16*>(dK),
+                                           static_cast<__nv_bfloat16*>(dV), n, n_pad, scale,
+                                           scale * 1.4426950408889634f, causal, ctl);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+int launch_q(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
+             const float* Dv, void* dQ, int BH, int n, int n_pad, float scale, int causal,
+             const KernelCtl& ctl, cudaStream_t st) {
+  using C = QCfg<D>;
+  CUtensorMap tq, tk, tv, tg;
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, C::BN) ||
+      !make_tmap_bf16(&tv, V, D, n, BH, 64, C::BN) || !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
+    return ATTN_ERR_CUDA;
+  auto kern = bwd_q_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  dim3 grid(ceil_div(n, C::BM), BH);
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, static_cast<__nv_bfloat16*>(dQ),
+                                           n, n_pad, scale, scale * 1.4426950408889634f, causal, ctl);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
+                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV, int BH,
+                     int n, int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                     cudaStream_t st) {
+#define ATTN_KV(DD, DQQ) \
+  return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal, ctl, st)
+  const bool dq = dQacc != nullptr;
+  switch (d) {
+    case 64: if (dq) { ATTN_KV(64, true); } else { ATTN_KV(64, false); }
+    case 128: if (dq) { ATTN_KV(128, true); } else { ATTN_KV(128, false); }
+    case 256: if (dq) return ATTN_ERR_UNSUPPORTED; ATTN_KV(256, false);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+#undef ATTN_KV
+}
+
+int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
+                    const float* LSE2, const float* Dv, void* dQ, int BH, int n, int n_pad, int d,
+                    float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+  switch (d) {
+    case 64: return launch_q<64>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
+    case 128: return launch_q<128>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
+    case 256: return launch_q<256>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,400 @@
+// fwd_tc.cu -- fused exact attention forward on the tcgen05 tensor cores.
+//
+// Computes O = softmax(scale Q K^T) V and LSE per row without writing the
+// n x n score matrix anywhere but tensor memory ("Chapter 3.1 -- The cost of
+// attention", section 5: tile Q, K, V into fast on-chip memory and combine
+// partial softmax statistics block by block; "Flash Attention:
+// Revolutionizing Transformer Efficiency", "The mathematics behind Flash
+// Attention", formulas 1-2).
+//
+// CTA = QT query tiles of 128 rows of one (b, h) head.  Roles:
+//   warp 0 (one lane)  TMA producer: Q tiles once, then K_j and V_j tiles
+//                      into separate shared-memory rings.
+//   warp 1 (one lane)  MMA issuer: S = Q K_j^T (SS-MMA into a TMEM slot),
+//                      O_t += P V_j (TS-MMA: P read from TMEM).
+//   warp 2             allocates / frees tensor memory.
+//   warpgroup 1 + t    softmax of query tile t: thread r owns row r (TMEM
+//                      lane r).  Loads its S row, applies the causal/ragged
+//                      mask, updates the running max m and sum l (log2
+//                      domain), writes P = 2^(s*scale*log2e - m) as bf16 over
+//                      the S slot, rescales its O row in TMEM when m moved,
+//                      and finally writes O / l and LSE.
+// Units (t, j) are processed in the order j-major, t-minor; unit number k
+// uses S slot k % 2, so the tensor cores compute the next unit's S while the
+// current unit's softmax runs (two tiles ping-pong when QT = 2).
+//
+// The running-max rescale is skipped while the new maximum exceeds the kept
+// one by at most 8 (a factor 256 in P); both l and O are accumulated against
+// the same kept maximum, so the final O / l is unchanged.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+template <int D, int BN, int QT>
+struct FwdCfg {
+  static constexpr int BM = 128;
+  static constexpr int NKB = D / 64;            // 64-wide (128 B) column boxes
+  static constexpr int KST = (D == 64) ? 3 : 2; // K and V ring depth
+  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t K_OFF = Q_OFF + QT * Q_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + KST * KV_BYTES;
+  static constexpr uint32_t BAR_OFF = V_OFF + KST * KV_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int S_COL = 0;               // two S slots of BN columns
+  static constexpr int O_COL = 2 * BN;          // QT accumulators of D columns
+  static constexpr int NTHREADS = 128 * (1 + QT);
+  static_assert(2 * BN + QT * D <= 512, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// Barrier indices inside the barrier block.
+enum : int { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17,
+             B_DRAIN = 19, B_COUNT = 20 };
+
+struct TileInfo {
+  int last0, last1;   // last KV tile index each query tile needs (-1: none)
+};
+
+__device__ __forceinline__ int unit_pos(int t, int j, const TileInfo& ti) {
+  return min(j, ti.last0 + 1) + min(j, ti.last1 + 1) + ((t == 1 && j <= ti.last0) ? 1 : 0);
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i] * mul, v[2 * i + 1] * mul);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+template <int D, int BN, int QT>
+__global__ void __launch_bounds__(FwdCfg<D, BN, QT>::NTHREADS, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+              float* __restrict__ LSE, int n, float scale_log2, int causal, KernelCtl ctl) {
+  using C = FwdCfg<D, BN, QT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + C::BAR_OFF;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int ntile = gridDim.x;
+  const int cta = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int row0 = cta * (QT * C::BM);
+  const int nkv = (n + BN - 1) / BN;
+
+  TileInfo ti;
+  {
+    int last[2] = {-1, -1};
+    for (int t = 0; t < QT; ++t) {
+      const int r0 = row0 + t * C::BM;
+      if (r0 < n) last[t] = causal ? min(nkv - 1, (r0 + C::BM - 1) / BN) : nkv - 1;
+    }
+    ti.last0 = last[0];
+    ti.last1 = last[1];
+  }
+  const int jmax = max(ti.last0, ti.last1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bar(B_KF + s), 1);
+      mbar_init(bar(B_KE + s), 1);
+      mbar_init(bar(B_VF + s), 1);
+      mbar_init(bar(B_VE + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SF + s), 1);
+      mbar_init(bar(B_PF + s), 128);
+      mbar_init(bar(B_OD + s), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 2) tmem_alloc<512>(smem_u32(tmem_slot));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    if (QT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t qbytes = 0;
+      for (int t = 0; t < QT; ++t)
+        if (row0 + t * C::BM < n) qbytes += C::Q_BYTES;
+      mbar_expect_tx(bar(B_Q), qbytes);
+      for (int t = 0; t < QT; ++t) {
+        if (row0 + t * C::BM >= n) continue;
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_3d(sb + C::Q_OFF + t * C::Q_BYTES + kb * (C::BM * 128), &tmQ, kb * 64,
+                      row0 + t * C::BM, bh, bar(B_Q));
+      }
+      int last_k[C::KST], last_v[C::KST];
+      for (int s = 0; s < C::KST; ++s) last_k[s] = last_v[s] = -1;
+      for (int j = 0; j <= jmax; ++j) {
+        const int s = j % C::KST;
+        const uint32_t ph = ((j / C::KST) & 1) ^ 1;
+        if (!mbar_wait(bar(B_KE + s), ph, abort_flag, ctl, SITE_FWD_KV_EMPTY)) break;
+        mbar_expect_tx(bar(B_KF + s), C::KV_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, j * BN, bh,
+                      bar(B_KF + s));
+        last_k[s] = j;
+        if (!mbar_wait(bar(B_VE + s), ph, abort_flag, ctl, SITE_FWD_KV_EMPTY)) break;
+        mbar_expect_tx(bar(B_VF + s), C::KV_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_3d(sb + C::V_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmV, kb * 64, j * BN, bh,
+                      bar(B_VF + s));
+        last_v[s] = j;
+      }
+      if (*abort_flag) {   // let issued copies land before the CTA may exit
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_Q), 0, &no_abort, ctl, SITE_FWD_LOAD_Q);
+        for (int s = 0; s < C::KST; ++s) {
+          if (last_k[s] >= 0)
+            mbar_wait(bar(B_KF + s), (last_k[s] / C::KST) & 1, &no_abort, ctl, SITE_FWD_K_FULL);
+          if (last_v[s] >= 0)
+            mbar_wait(bar(B_VF + s), (last_v[s] / C::KST) & 1, &no_abort, ctl, SITE_FWD_V_FULL);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16(C::BM, BN, false, false);   // Q, K both K-major
+      constexpr uint32_t idesc_o = idesc_bf16(C::BM, D, false, true);     // P (TMEM), V MN-major
+      auto need = [&](int t, int j) { return j <= (t == 0 ? ti.last0 : ti.last1); };
+      int total = 0;
+      for (int t = 0; t < QT; ++t) total += (t == 0 ? ti.last0 : ti.last1) + 1;
+      // Cursor over the needed units (t, j), j-major / t-minor.
+      struct Cur { int t, j; };
+      auto advance = [&](Cur& c) {
+        do {
+          if (++c.t == QT) { c.t = 0; ++c.j; }
+        } while (c.j <= jmax && !need(c.t, c.j));
+      };
+      Cur cs{0, 0}, cp{0, 0};   // next unit to get S, next unit to get PV
+      if (!need(0, 0)) { advance(cs); advance(cp); }
+      auto first_user = [&](int t, int j) { return t == 0 || !need(0, j); };
+      auto last_user = [&](int t, int j) { return t == QT - 1 || !need(QT - 1, j); };
+      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      auto issue_s = [&](int k) -> bool {
+        const int t = cs.t, j = cs.j;
+        advance(cs);
+        const int s = j % C::KST;
+        if (first_user(t, j)) {
+          if (!mbar_wait(bar(B_KF + s), (j / C::KST) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
+            return false;
+        }
+        tc_fence_after();
+        const uint32_t qa = sb + C::Q_OFF + t * C::Q_BYTES;
+        const uint32_t ka = sb + C::K_OFF + s * C::KV_BYTES;
+        const uint32_t dst = tmem + C::S_COL + (k & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(qa + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(ka + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(dst, a, b, idesc_s, kk > 0);
+        }
+        tc_commit(bar(B_SF + (k & 1)));
+        if (last_user(t, j)) tc_commit(bar(B_KE + s));
+        return true;
+      };
+      if (ok && total > 0) ok = issue_s(0);
+      if (ok && total > 1) ok = issue_s(1);
+      for (int k = 0; ok && k < total; ++k) {
+        const int t = cp.t, j = cp.j;
+        advance(cp);
+        const int s = j % C::KST;
+        if (!mbar_wait(bar(B_PF + (k & 1)), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
+        if (first_user(t, j)) {
+          if (!mbar_wait(bar(B_VF + s), (j / C::KST) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
+        }
+        tc_fence_after();
+        const uint32_t pa = tmem + C::S_COL + (k & 1) * BN;       // P: bf16 pairs, BN/2 columns
+        const uint32_t va = sb + C::V_OFF + s * C::KV_BYTES;
+        const uint32_t dst = tmem + C::O_COL + t * D;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(va + kk * 2048, BN * 128, 1024);
+          mma_ts(dst, pa + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(B_OD + t));
+        if (last_user(t, j)) tc_commit(bar(B_VE + s));
+        if (k + 2 < total) ok = issue_s(k + 2);
+      }
+      if (*abort_flag) {
+        tc_commit(bar(B_DRAIN));
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_DRAIN), 0, &no_abort, ctl, SITE_FWD_O_DONE);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax
+    if (QT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    const int t = (warp >> 2) - 1;
+    const int q = warp & 3;                       // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const int row = row0 + t * C::BM + r;
+    const int last = (t == 0) ? ti.last0 : ti.last1;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j <= last; ++j) {
+      const int k = unit_pos(t, j, ti);
+      const int slot = k & 1;
+      ok = mbar_wait(bar(B_SF + slot), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_S_FULL);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sa = tmem + lane_off + C::S_COL + slot * BN;
+      float s[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(sa + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(rr[i]);
+      }
+      const int col0 = j * BN;
+      const bool need_mask = (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
+      if (need_mask) {
+        const int lim = causal ? min(n, row + 1) : n;   // columns < lim are kept
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (col0 + c >= lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_cand = mx * scale_log2;
+      const float m_new = (m_cand > m + 8.0f) ? m_cand : m;
+      const float alpha = ex2(m - m_new);   // 0 on the first tile (m = -inf)
+      float rs = 0.f;
+      const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(s[c0 + 2 * i], scale_log2, -m_new));
+          const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale_log2, -m_new));
+          rs += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(pa + c0 / 2, pk);
+      }
+      tmem_st_wait();
+      l = l * alpha + rs;
+      // Wait for PV of tile j-1 every iteration: a parity wait is only
+      // unambiguous while the waiter is at most one phase behind.
+      if (j > 0) {
+        ok = mbar_wait(bar(B_OD + t), (j - 1) & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      // Rescale this row of O when its kept maximum moved.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        tc_fence_after();
+        const uint32_t oa = tmem + lane_off + C::O_COL + t * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(oa + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st32(oa + c0, rr);
+        }
+        tmem_st_wait();
+      }
+      m = m_new;
+      tc_fence_before();
+      mbar_arrive(bar(B_PF + slot));
+    }
+    if (ok && last >= 0) {
+      ok = mbar_wait(bar(B_OD + t), last & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const uint32_t oa = tmem + lane_off + C::O_COL + t * D;
+        const size_t obase = ((size_t)bh * n + row) * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(oa + c0, rr);
+          tmem_ld_wait();
+          if (row < n) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
+            store_row_bf16(O + obase + c0, v, inv);
+          }
+        }
+        if (row < n) LSE[(size_t)bh * n + row] = (m + __log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc<512>(tmem);
+}
+
+template <int D, int BN, int QT>
+int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
+               float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+  using C = FwdCfg<D, BN, QT>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, BN) ||
+      !make_tmap_bf16(&tv, V, D, n, BH, 64, BN))
+    return ATTN_ERR_CUDA;
+  auto kern = fwd_tc_kernel<D, BN, QT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  dim3 grid(ceil_div(n, QT * C::BM), BH);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, n,
+                                           scale_log2, causal, ctl);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
+                  int d, float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+  switch (d) {
+    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
+    case 128: return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
+    case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,245 @@
+// gemm_tc.cu -- batched bf16 GEMM on the 5th-generation tensor cores.
+//
+//   C[b] = alpha * A[b] (M x K) * B[b] (K x N), fp32 accumulation in TMEM.
+//
+// One CTA computes one 128 x BN tile of C.  Warp 0 (one lane) streams 64-wide
+// K blocks of A and B into a 4-stage shared-memory ring with TMA; warp 1
+// (one lane) issues tcgen05.mma (M=128, N=BN, K=16) per K block and releases
+// each stage with tcgen05.commit; then all four warps read the accumulator
+// back with tcgen05.ld (thread t <-> row t) and store C.  A and B may each be
+// K-major or MN-major in global memory: the shared-memory descriptors and the
+// transpose bits of the instruction descriptor absorb the difference, so no
+// operand is ever transposed in memory.  This GEMM carries every n x n and
+// n x d product of the materialise-P comparison path.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+
+template <int BN>
+struct GemmLayout {
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr uint32_t B_BYTES = BN * kBK * 2;
+  static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+  static constexpr uint32_t BAR_OFF = kStages * STAGE;
+  static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;  // barriers + slack for 1 KB alignment
+};
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Descriptor of one 16-deep K slice `kk` of a 64-deep staged K block.
+//  K-major: rows of 64 K elements (128 B); the slice starts 32 B further.
+//  MN-major: rows of 64 M/N elements, one per k; the slice starts 16 rows
+//  (2048 B) further; 64-wide M/N blocks are `mn_block_bytes` apart.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int kk,
+                                                 uint32_t mn_block_bytes) {
+  return kmajor ? sdesc_sw128(base + kk * 32, 16, 1024)
+                : sdesc_sw128(base + kk * 2048, mn_block_bytes, 1024);
+}
+
+template <int BN, bool A_K, bool B_K, bool C_F32>
+__global__ void __launch_bounds__(128, 1)
+gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                 void* __restrict__ C, int M, int N, int K, float alpha, KernelCtl ctl) {
+  using L = GemmLayout<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1k(smem_raw);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t acc_bar = bar0 + 8u * (2 * kStages);
+  const uint32_t drain_bar = acc_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 136);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN, b = blockIdx.z;
+  const int nkb = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tB);
+  }
+  if (warp == 2) tmem_alloc<BN>(smem_u32(tmem_slot));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int issued_last[kStages];
+    for (int s = 0; s < kStages; ++s) issued_last[s] = -1;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(empty(s), ((kb / kStages) & 1) ^ 1, abort_flag, ctl, SITE_GEMM_EMPTY)) break;
+      const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
+      mbar_expect_tx(full(s), L::STAGE);
+      if (A_K) {
+        tma_load_3d(sa, &tA, kb * kBK, m0, b, full(s));
+      } else {
+        tma_load_3d(sa, &tA, m0, kb * kBK, b, full(s));
+        tma_load_3d(sa + 8192, &tA, m0 + 64, kb * kBK, b, full(s));
+      }
+      if (B_K) {
+        tma_load_3d(sb, &tB, kb * kBK, n0, b, full(s));
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < BN / 64; ++nb) tma_load_3d(sb + nb * 8192, &tB, n0 + nb * 64, kb * kBK, b, full(s));
+      }
+      issued_last[s] = kb;
+    }
+    if (*abort_flag) {
+      // Let every copy already issued land before the CTA can exit.
+      for (int s = 0; s < kStages; ++s)
+        if (issued_last[s] >= 0) {
+          KernelCtl c2 = ctl;
+          volatile int no_abort = 0;
+          mbar_wait(full(s), (issued_last[s] / kStages) & 1, &no_abort, c2, SITE_GEMM_FULL);
+        }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kBM, BN, !A_K, !B_K);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(full(s), (kb / kStages) & 1, abort_flag, ctl, SITE_GEMM_FULL)) break;
+      tc_fence_after();
+      const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        mma_ss(tmem, operand_desc(sa, A_K, kk, 8192), operand_desc(sb, B_K, kk, 8192), idesc,
+               (kb | kk) != 0);
+      }
+      tc_commit(empty(s));
+    }
+    tc_commit(acc_bar);
+    if (*abort_flag) {
+      tc_commit(drain_bar);
+      volatile int no_abort = 0;
+      mbar_wait(drain_bar, 0, &no_abort, ctl, SITE_GEMM_ACC);
+    }
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> registers -> global
+  const bool ok = mbar_wait(acc_bar, 0, abort_flag, ctl, SITE_GEMM_ACC);
+  tc_fence_after();
+  if (ok) {
+    const int row = m0 + warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c0, r);
+      tmem_ld_wait();
+      const int col = n0 + c0;
+      if (row < M && col < N) {
+        if (C_F32) {
+          float* dst = static_cast<float*>(C) + ((size_t)b * M + row) * N + col;
+          if (col + 32 <= N && (N & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) =
+                  make_float4(alpha * __uint_as_float(r[i]), alpha * __uint_as_float(r[i + 1]),
+                              alpha * __uint_as_float(r[i + 2]), alpha * __uint_as_float(r[i + 3]));
+          } else {
+            for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = alpha * __uint_as_float(r[i]);
+          }
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + ((size_t)b * M + row) * N + col;
+          if (col + 32 <= N && (N & 7) == 0) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(alpha * __uint_as_float(r[2 * i]),
+                                  alpha * __uint_as_float(r[2 * i + 1]));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(dst + 8 * i) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          } else {
+            for (int i = 0; i < 32 && col + i < N; ++i)
+              dst[i] = __float2bfloat16_rn(alpha * __uint_as_float(r[i]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc<BN>(tmem);
+}
+
+template <int BN, bool A_K, bool B_K, bool C_F32>
+int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int batch, int M,
+                   int N, int K, float alpha, const KernelCtl& ctl, cudaStream_t st) {
+  auto kern = gemm_bf16_kernel<BN, A_K, B_K, C_F32>;
+  constexpr int smem = GemmLayout<BN>::TOTAL;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  dim3 grid(ceil_div(N, BN), ceil_div(M, kBM), batch);
+  kern<<<grid, 128, smem, st>>>(ta, tb, C, M, N, K, alpha, ctl);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int BN>
+int dispatch_bn(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int batch, int M, int N,
+                int K, bool ak, bool bk, bool cf, float alpha, const KernelCtl& ctl,
+                cudaStream_t st) {
+#define ATTN_GEMM_CASE(AK, BK, CF)                                                    \
+  if (ak == AK && bk == BK && cf == CF)                                               \
+    return launch_variant<BN, AK, BK, CF>(ta, tb, C, batch, M, N, K, alpha, ctl, st);
+  ATTN_GEMM_CASE(true, true, true)
+  ATTN_GEMM_CASE(true, false, true)
+  ATTN_GEMM_CASE(false, true, true)
+  ATTN_GEMM_CASE(false, false, true)
+  ATTN_GEMM_CASE(true, true, false)
+  ATTN_GEMM_CASE(true, false, false)
+  ATTN_GEMM_CASE(false, true, false)
+  ATTN_GEMM_CASE(false, false, false)
+#undef ATTN_GEMM_CASE
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, int N, int K,
+                     bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
+                     cudaStream_t st) {
+  const int BN = N > 128 ? 256 : 128;
+  CUtensorMap ta, tb;
+  // A: K-major [b][M][K] (x = K) or MN-major [b][K][M] (x = M)
+  bool ok = a_kmajor ? make_tmap_bf16(&ta, A, K, M, batch, 64, kBM)
+                     : make_tmap_bf16(&ta, A, M, K, batch, 64, kBK);
+  // B: K-major [b][N][K] (x = K) or MN-major [b][K][N] (x = N)
+  ok = ok && (b_kmajor ? make_tmap_bf16(&tb, B, K, N, batch, 64, BN)
+                       : make_tmap_bf16(&tb, B, N, K, batch, 64, kBK));
+  if (!ok) return ATTN_ERR_CUDA;
+  return BN == 256 ? dispatch_bn<256>(ta, tb, C, batch, M, N, K, a_kmajor, b_kmajor, c_f32, alpha,
+                                      ctl, st)
+                   : dispatch_bn<128>(ta, tb, C, batch, M, N, K, a_kmajor, b_kmajor, c_f32, alpha,
+                                      ctl, st);
+}
+
+}  // namespace attn

@@ -1,0 +1,83 @@
+// host.cu -- host-side helpers: TMA tensor-map encoding and the device status
+// word shared by every kernel of the library.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace attn {
+
+// First device-side error: [0] = attn_status_t code, [1] = wait site.
+__device__ int g_status_word[2];
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                    uint32_t box_x, uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {x, y, z};
+  const cuuint64_t strides[2] = {x * 2, x * y * 2};   // bytes, dims 1..2
+  const cuuint32_t box[3] = {box_x, box_y, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Address of the status word, looked up once per device.
+static int* status_word_ptr() {
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static uint64_t g_timeout_ns = 2000000000ull;   // 2 s per barrier wait
+
+KernelCtl default_ctl() {
+  KernelCtl c;
+  c.err = status_word_ptr();
+  c.timeout_ns = g_timeout_ns;
+  return c;
+}
+
+int read_and_clear_status(cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* p = status_word_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, p, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h[0] != 0) {
+    const int z[2] = {0, 0};
+    if (cudaMemcpy(p, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return h[0];
+}
+
+}  // namespace attn

@@ -1,0 +1,63 @@
+// kernels.h -- internal launchers of libattn (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+// ---- tensor maps (host) ---------------------------------------------------
+// A 3-D bf16 tensor map over [z][y][x] (x innermost, contiguous), with the
+// 128-byte swizzle and zero fill outside the tensor.  box_x * 2 must be 128.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                    uint32_t box_x, uint32_t box_y);
+
+KernelCtl default_ctl();
+
+// ---- fp32 SIMT path --------------------------------------------------------
+cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
+                           int BH, int n, int d, float scale, int causal, cudaStream_t st);
+cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH, int n, int d,
+                             cudaStream_t st);
+cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, const float* dO,
+                                const float* LSE, const float* Dv, float* dK, float* dV, int BH,
+                                int n, int d, float scale, int causal, cudaStream_t st);
+cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, const float* dO,
+                              const float* LSE, const float* Dv, float* dQ, int BH, int n, int d,
+                              float scale, int causal, cudaStream_t st);
+
+// ---- bf16 helpers ------------------------------------------------------------
+cudaError_t launch_delta_bf16(const void* O, const void* dO, const float* LSE, float* Dv,
+                              float* LSE2, float* dQacc, int BH, int n, int n_pad, int d,
+                              cudaStream_t st);
+cudaError_t launch_dq_convert(const float* acc, void* dQ, size_t elems, cudaStream_t st);
+
+// ---- tensor-core kernels -------------------------------------------------------
+int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, int N, int K,
+                     bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
+                     cudaStream_t st);
+
+int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
+                  int d, float scale, int causal, const KernelCtl& ctl, cudaStream_t st);
+
+// Key-tile backward: dK, dV (and, with dQacc != nullptr, atomic dQ shares).
+int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
+                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV, int BH,
+                     int n, int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                     cudaStream_t st);
+// Query-tile backward: dQ with no atomics.
+int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
+                    const float* LSE2, const float* Dv, void* dQ, int BH, int n, int n_pad, int d,
+                    float scale, int causal, const KernelCtl& ctl, cudaStream_t st);
+
+// ---- materialise-P row kernels ----------------------------------------------------
+cudaError_t launch_mat_softmax(const float* S, void* P, float* LSE, int BH, int n, float scale,
+                               int causal, cudaStream_t st);
+cudaError_t launch_mat_dsoftmax(const void* P, const float* dP, const float* Dv, void* dS, int BH,
+                                int n, cudaStream_t st);
+
+}  // namespace attn

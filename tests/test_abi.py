@@ -1,0 +1,135 @@
+"""Host-side tests of the C ABI: the library builds, loads and exports every
+declared entry point; argument checks return the documented codes without
+touching a GPU; workspace sizes follow the documented layout."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from io_aware_exact_05_gb300 import attn
+    from io_aware_exact_05_gb300.build import build
+
+    if not os.path.exists(attn.lib_path()):
+        build()
+    return attn.lib()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", txt)))
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status",
+              "attn_strerror", "attn_mat_fwd", "attn_mat_bwd", "attn_gemm_bf16"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_strerror_and_version(L):
+    from io_aware_exact_05_gb300 import attn
+
+    assert attn.attn_strerror(0) == "success"
+    for c in range(1, 6):
+        assert attn.attn_strerror(c) not in ("", "unknown status code")
+    assert attn.attn_strerror(99) == "unknown status code"
+    assert "sm_103a" in attn.attn_version()
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced
+MIS = ctypes.c_void_p((1 << 20) + 8)     # misaligned
+
+
+def _fwd(L, *, p=FAKE, B=1, H=1, n=128, d=64, dt=0, scale=0.125, causal=0):
+    return L.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, B, H, n, d, dt, scale, causal, None)
+
+
+def test_fwd_argument_checks(L):
+    assert _fwd(L, p=ctypes.c_void_p(0)) == 1
+    assert _fwd(L, p=MIS) == 1
+    assert _fwd(L, B=0) == 1
+    assert _fwd(L, n=0) == 1
+    assert _fwd(L, d=0) == 1
+    assert _fwd(L, causal=2) == 1
+    assert _fwd(L, scale=float("nan")) == 1
+    assert _fwd(L, scale=float("inf")) == 1
+    assert _fwd(L, dt=7) == 1
+    assert _fwd(L, d=96) == 2                # bf16 head dims are 64, 128, 256
+    assert _fwd(L, d=512, dt=1) == 2         # fp32 path: d <= 256
+    assert _fwd(L, B=300, H=300) == 2        # B*H beyond the grid's head axis
+
+
+def _ws(L, B, H, n, d, dt, causal, mode):
+    return L.attn_bwd_workspace_size(B, H, n, d, dt, causal, mode)
+
+
+def _rup(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def test_workspace_sizes(L):
+    B, H, n, d = 2, 3, 1000, 128
+    BH, n_pad = B * H, 1024
+    stats = 2 * _rup(BH * n_pad * 4)
+    assert _ws(L, B, H, n, d, 0, 1, 1) == stats + _rup(BH * n * d * 4)   # atomic
+    assert _ws(L, B, H, n, d, 0, 1, 2) == stats                          # pass
+    assert _ws(L, B, H, n, d, 0, 1, 0) == _ws(L, B, H, n, d, 0, 1, 1)    # auto = atomic
+    assert _ws(L, B, H, n, 256, 0, 0, 0) == stats                        # d=256: pass
+    assert _ws(L, B, H, n, 256, 0, 0, 1) == 0                            # not supported
+    assert _ws(L, B, H, n, 100, 1, 0, 0) == _rup(BH * n * 4)             # fp32: D only
+    assert _ws(L, B, H, n, 96, 0, 0, 0) == 0
+    assert _ws(L, 0, H, n, d, 0, 0, 0) == 0
+    # materialise-P: S/dP fp32 + P/dS bf16 + D + LSE2
+    nn = BH * 1024 * 1024
+    assert L.attn_mat_workspace_size(B, H, 1024, 64) == (
+        _rup(nn * 4) + _rup(nn * 2) + 2 * _rup(BH * 1024 * 4))
+    assert L.attn_mat_workspace_size(B, H, 1001, 64) == 0               # n % 8 != 0
+
+
+def test_bwd_argument_checks(L):
+    ws = ctypes.c_void_p(1 << 24)
+    args = [FAKE] * 9
+
+    def call(*, d=128, dt=0, mode=0, wsb=1 << 30, wsp=ws, scale=0.1):
+        return L.attn_bwd(*args, 1, 2, 256, d, dt, scale, 1, mode, wsp, wsb, None)
+
+    assert call(mode=9) == 1
+    assert call(d=96) == 2
+    assert call(d=256, mode=1) == 2
+    assert call(wsb=16) == 3                       # workspace too small
+    assert call(wsp=ctypes.c_void_p(0)) == 3       # no workspace
+    assert call(wsp=ctypes.c_void_p((1 << 24) + 16)) == 3   # not 256-byte aligned
+    assert call(scale=float("nan")) == 1
+    bad = [FAKE] * 8 + [ctypes.c_void_p(0)]
+    assert L.attn_bwd(*bad, 1, 2, 256, 128, 0, 0.1, 1, 0, ws, 1 << 30, None) == 1
+
+
+def test_gemm_argument_checks(L):
+    g = L.attn_gemm_bf16
+    assert g(FAKE, FAKE, FAKE, 1, 128, 128, 60, 1, 1, 1, 1.0, None) == 2   # K % 8
+    assert g(FAKE, FAKE, FAKE, 1, 100, 128, 64, 0, 1, 1, 1.0, None) == 2   # MN-major A, M % 8
+    assert g(FAKE, FAKE, FAKE, 1, 128, 100, 64, 1, 0, 1, 1.0, None) == 2   # MN-major B, N % 8
+    assert g(FAKE, FAKE, FAKE, 0, 128, 128, 64, 1, 1, 1, 1.0, None) == 1
+    assert g(ctypes.c_void_p(0), FAKE, FAKE, 1, 128, 128, 64, 1, 1, 1, 1.0, None) == 1
+
+
+def test_flop_counts():
+    from io_aware_exact_05_gb300.flops import attention_flops
+
+    f = attention_flops(2, 16, 8192, 128, causal=True)
+    assert f["fwd"] == 4 * 2 * 16 * 8192 ** 2 * 128 // 2
+    assert f["bwd"] == 10 * 2 * 16 * 8192 ** 2 * 128 // 2
+    assert abs(f["bwd"] / 1e12 - 1.374) < 1e-3

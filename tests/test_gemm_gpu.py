@@ -1,0 +1,47 @@
+"""The tcgen05/TMA GEMM (the building block of the materialise-P path)
+against a float64 CPU matrix product, for every operand major-ness."""
+
+import pytest
+import torch
+
+from parity_util import relerr
+
+pytestmark = pytest.mark.gpu
+
+
+def _operands(batch, M, N, K, ak, bk, seed):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(batch, M, K, generator=g).to(torch.bfloat16)   # logical A (M x K)
+    B = torch.randn(batch, K, N, generator=g).to(torch.bfloat16)   # logical B (K x N)
+    a_st = A if ak else A.transpose(1, 2).contiguous()              # [M][K] or [K][M]
+    b_st = B.transpose(1, 2).contiguous() if bk else B              # [N][K] or [K][N]
+    ref = torch.matmul(A.double(), B.double())
+    return a_st, b_st, ref
+
+
+@pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 1), (0, 0)])
+@pytest.mark.parametrize("batch,M,N,K", [(1, 128, 128, 64), (2, 256, 256, 192),
+                                         (3, 200, 136, 72), (1, 128, 64, 128),
+                                         (2, 384, 512, 320)])
+@pytest.mark.parametrize("c_f32", [True, False])
+def test_gemm(cuda_dev, ak, bk, batch, M, N, K, c_f32):
+    from io_aware_exact_05_gb300 import attn
+
+    a, b, ref = _operands(batch, M, N, K, ak, bk, seed=M * 7 + N + K + ak * 2 + bk)
+    c = torch.full((batch, M, N), float("nan"), device=cuda_dev,
+                   dtype=torch.float32 if c_f32 else torch.bfloat16)
+    attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, ak, bk, alpha=0.5)
+    assert attn.attn_status() == 0
+    err = relerr(c, 0.5 * ref)
+    assert err <= (1e-5 if c_f32 else 1e-2), err
+
+
+def test_gemm_ragged_kmajor(cuda_dev):
+    from io_aware_exact_05_gb300 import attn
+
+    batch, M, N, K = 2, 130, 70, 40
+    a, b, ref = _operands(batch, M, N, K, 1, 1, seed=5)
+    c = torch.full((batch, M, N), float("nan"), device=cuda_dev)
+    attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, 1, 1)
+    assert attn.attn_status() == 0
+    assert relerr(c, ref) <= 1e-5
