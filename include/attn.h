@@ -141,6 +141,32 @@ ATTN_API int attn_bwd_dq(const void* Q, const void* K, const void* V,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_noalloc -- the backward pass for callers that cannot allocate.
+ * The pages have no counterpart to this entry point; it is a deployment aid.
+ * Some callers cannot pass a workspace: they hold no device allocator of
+ * their own, or their device-memory budget is fixed at start-up, or they must
+ * not call cudaMalloc where they run the backward because it can block the
+ * host or synchronise the device.  This variant takes the same tensors as
+ * attn_bwd but keeps its scratch (the LSE and D row statistics) in a fixed
+ * 16 MiB device array inside the library, present on every GPU that loads
+ * the library until the process exits.  It allocates nothing.
+ *   - Computes dQ with the query-tile pass (bf16 results equal attn_bwd with
+ *     ATTN_DQ_PASS); fp32 uses the SIMT kernels.
+ *   - Size limit: bf16 B*H*n_pad <= 2,097,152 (n_pad = n rounded up to 128),
+ *     fp32 B*H*n <= 4,194,304; larger problems return ATTN_ERR_WORKSPACE
+ *     before any launch.
+ *   - All calls share the array.  Calls whose work overlaps on the GPU (two
+ *     streams, or two threads without ordering) race: keep them on one stream
+ *     or synchronise in between.  Nothing in the array needs to start at zero.
+ *   - The first call on each device looks up the array's address on that
+ *     device; make that first call before capturing any stream.
+ */
+ATTN_API int attn_bwd_noalloc(const void* Q, const void* K, const void* V,
+             const void* O, const void* dO, const float* LSE, void* dQ,
+             void* dK, void* dV, int B, int H, int n, int d, attn_dtype dtype,
+             float scale, int causal, void* stream);
+
+/*
  * Materialise-P comparison path (bf16 only, d in {64,128,256}).  The plainest
  * reading of the small-cache algorithm of "On the fine-grained I/O
  * complexity of attention backward passes" (Methodology step 3: it reads
