@@ -659,7 +659,9 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
   const bool dq = dQacc != nullptr;
   switch (d) {
     case 64: if (dq) { ATTN_KV(64, true); } else { ATTN_KV(64, false); }
-    case 128: if (dq) { ATTN_KV(128, true); } else { ATTN_KV(128, false); }
+    case 128:
+      return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal,
+                                 ctl, st);
     case 256: if (dq) return ATTN_ERR_UNSUPPORTED; ATTN_KV(256, false);
     default: return ATTN_ERR_UNSUPPORTED;
   }

@@ -15,6 +15,9 @@ namespace attn {
 // 128-byte swizzle and zero fill outside the tensor.  box_x * 2 must be 128.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
                     uint32_t box_x, uint32_t box_y);
+// A 3-D fp32 tensor map over [z][y][x] with no swizzle (for reduce-add tiles).
+bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                   uint32_t box_x, uint32_t box_y);
 
 KernelCtl default_ctl();
 
@@ -49,6 +52,12 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
                      const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV, int BH,
                      int n, int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
                      cudaStream_t st);
+// Key-tile backward for d = 128, pipelined two query tiles deep (dQ shares
+// reduced into dQacc with TMA bulk reduce-add when dQacc != nullptr).
+int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
+                        const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                        int BH, int n, int n_pad, float scale, int causal, const KernelCtl& ctl,
+                        cudaStream_t st);
 // Query-tile backward: dQ with no atomics.
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
                     const float* LSE2, const float* Dv, void* dQ, int BH, int n, int n_pad, int d,
