@@ -1,32 +1,33 @@
-// bwd_kv128.cu -- key-tile attention backward for head dim 128, software-
-// pipelined two query tiles deep.
+// bwd_kv128.cu -- key-tile attention backward for head dim 128.
 //
-// One CTA owns 128 keys of one head (the TMEM lanes) and walks the query
-// tiles (64 queries each) that can see them.  For every query tile u, with
-// c = scale * log2(e) and LSE2 = LSE * log2(e):
-//   S^T  = K Q_u^T                (SS-MMA, M = 128 keys, N = 64 queries)
+// One CTA owns 128 keys of one head (the TMEM lanes) and walks the 128-query
+// tiles that can see them.  For every query tile u, with c = scale * log2(e)
+// and LSE2 = LSE * log2(e):
+//   S^T  = K Q_u^T                (SS-MMA, M = 128 keys, N = 128 queries)
 //   P^T  = 2^(S^T c - LSE2)       (registers; bf16 copy back into TMEM)
 //   dV  += P^T dO_u               (TS-MMA: A = P^T read from TMEM)
 //   dP^T = V dO_u^T               (SS-MMA)
 //   dS^T = P^T o (dP^T - D)       (registers; bf16 copy into shared memory)
-//   dK  += dS^T Q_u               (SS-MMA: A = dS^T, K-major over queries)
-//   dQ_u^T = K^T dS^T             (SS-MMA: M = d on the lanes, N = 64 queries)
+//   dK  += dS^T Q_u               (SS-MMA: A = dS^T, K-major over the queries)
+//   dQ_u = dS K                   (SS-MMA: A = dS, MN-major; M = 128 queries)
 // These are the chain-rule steps of the backward pass that recomputes the
 // attention matrix instead of storing it ("Chapter 3.1 -- The cost of
 // attention", section 5; "Flash Attention: Revolutionizing Transformer
 // Efficiency", key idea 2).
 //
-// Tensor memory (512 columns): dV [0,128), dK [128,256), S^T in two 64-column
-// slots [256,384), dP^T [384,448), dQ^T [448,512).  Shared memory: K and V
-// tiles, a 3-deep ring of (Q tile, LSE2, D), a 2-deep ring of dO tiles, two
-// dS^T buffers and a 64 x 128 fp32 dQ staging tile.
+// Why 128-query tiles: an SS-MMA of M = 128 rows reads (128 + N) x 16 x 2
+// bytes of shared memory per 2 x 128 x N x 16 FLOPs.  At N = 64 the tensor
+// cores' operand traffic exceeds their MMA time; at N = 128 it stays below.
 //
-// The MMA issuer runs, per tile u,  dV(u) | dP(u+1) | dK(u), dQ^T(u) | S(u+2):
-// S of the tile after next is already in TMEM while the compute warps finish
-// tile u, so they go from dS(u) straight to the exponentials of u+1.  The dQ
-// warpgroup reads each dQ^T tile out of TMEM, stages it as fp32 [64][128] in
-// shared memory and adds it into the fp32 dQ accumulator with one TMA bulk
-// reduce-add.  Every wait is bounded (mbar_wait).
+// Tensor memory (512 columns): dV [0,128), dK [128,256), S^T [256,384),
+// dP^T [384,512).  The dQ tile reuses the dP^T columns once the compute
+// warps have read dP^T, so S of the next tile is issued right after dV and
+// its exponentials overlap this tile's dK and dQ products.  dS^T is written
+// over the dO tile of its stage (after dV has consumed dO).  The dQ
+// warpgroup (given 176 registers by setmaxnreg) pulls the whole fp32 dQ tile
+// out of TMEM, releases the columns, and adds the tile into the global fp32
+// accumulator as four 128 x 32 boxes staged in shared memory (128-byte
+// swizzle), one TMA bulk reduce-add each.  Every wait is bounded (mbar_wait).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -52,40 +53,33 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
     reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
-template <bool DQ>
 struct Kv128 {
-  static constexpr int D = 128, BNK = 128, BM = 64, NKB = 2;
-  static constexpr int QST = 3, GST = 2;
+  static constexpr int D = 128, BNK = 128, BM = 128, NKB = 2, STG = 2;
   static constexpr uint32_t KV_BYTES = BNK * D * 2;           // 32 KB
-  static constexpr uint32_t QT_BYTES = BM * D * 2;            // 16 KB
-  static constexpr uint32_t QSLOT = QT_BYTES + 1024;          // Q + LSE2 (+0) + D (+512)
-  static constexpr uint32_t DS_BYTES = BM * BNK * 2;          // 16 KB
+  static constexpr uint32_t QT_BYTES = BM * D * 2;            // 32 KB
+  static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024;      // Q, dO, LSE2 (+0), D (+512)
   static constexpr uint32_t K_OFF = 0, V_OFF = KV_BYTES;
-  static constexpr uint32_t Q_OFF = 2 * KV_BYTES;
-  static constexpr uint32_t G_OFF = Q_OFF + QST * QSLOT;
-  static constexpr uint32_t DS_OFF = G_OFF + GST * QT_BYTES;
-  static constexpr uint32_t QS_OFF = DS_OFF + 2 * DS_BYTES;
-  static constexpr uint32_t QS_BYTES = DQ ? BM * D * 4 : 0;
+  static constexpr uint32_t ST_OFF = 2 * KV_BYTES;
+  static constexpr uint32_t QS_OFF = ST_OFF + STG * STAGE;     // dQ staging: [128][32] fp32
+  static constexpr uint32_t QS_BYTES = BM * 32 * 4;             // 16 KB, 128-byte swizzle
   static constexpr uint32_t BAR_OFF = QS_OFF + QS_BYTES;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
-  static constexpr int DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384, DQ_COL = 448;
-  static constexpr int NTHREADS = DQ ? 512 : 384;
+  static constexpr int DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// barrier indices
-enum : int { P_KV = 0, P_QF = 1, P_QE = 4, P_GF = 7, P_GE = 9, P_SF = 11, P_DPF = 13, P_PR = 14,
-             P_DPE = 15, P_DSR = 16, P_DSE = 17, P_DQF = 19, P_DQE = 20, P_ACC = 21, P_DRAIN = 22 };
+enum : int { B_KV = 0, B_QF = 1, B_QE = 3, B_SF = 5, B_DPF = 6, B_PR = 7, B_DVD = 8, B_DSR = 9,
+             B_DQF = 10, B_DQE = 11, B_ACC = 12, B_DRAIN = 13 };
 
 template <bool DQ>
-__global__ void __launch_bounds__(Kv128<DQ>::NTHREADS, 1)
+__global__ void __launch_bounds__(DQ ? 512 : 384, 1)
 bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                 const __grid_constant__ CUtensorMap tmdQ, const float* __restrict__ LSE2,
-                 const float* __restrict__ Dv, __nv_bfloat16* __restrict__ dK,
-                 __nv_bfloat16* __restrict__ dV, int n, int n_pad, float scale, float scale_log2,
-                 int causal, KernelCtl ctl) {
-  using C = Kv128<DQ>;
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmdQ, const float* __restrict__ LSE2, const float* __restrict__ Dv,
+                  float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
+                  __nv_bfloat16* __restrict__ dV, int n, int n_pad, float scale, float scale_log2,
+                  int causal, KernelCtl ctl) {
+  using C = Kv128;
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1k(smem_raw);
@@ -100,21 +94,20 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
-  const int cnt = nq - i_start;   // query tiles that see these keys (>= 1)
+  const int cnt = nq - i_start;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(P_KV), 1);
-    for (int s = 0; s < C::QST; ++s) { mbar_init(bar(P_QF + s), 1); mbar_init(bar(P_QE + s), 1); }
-    for (int s = 0; s < C::GST; ++s) { mbar_init(bar(P_GF + s), 1); mbar_init(bar(P_GE + s), 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(bar(P_SF + s), 1); mbar_init(bar(P_DSE + s), 1); }
-    mbar_init(bar(P_DPF), 1);
-    mbar_init(bar(P_PR), 256);
-    mbar_init(bar(P_DPE), 256);
-    mbar_init(bar(P_DSR), 256);
-    mbar_init(bar(P_DQF), 1);
-    mbar_init(bar(P_DQE), 128);
-    mbar_init(bar(P_ACC), 1);
-    mbar_init(bar(P_DRAIN), 1);
+    mbar_init(bar(B_KV), 1);
+    for (int s = 0; s < C::STG; ++s) { mbar_init(bar(B_QF + s), 1); mbar_init(bar(B_QE + s), 1); }
+    mbar_init(bar(B_SF), 1);
+    mbar_init(bar(B_DPF), 1);
+    mbar_init(bar(B_PR), 256);
+    mbar_init(bar(B_DVD), 1);
+    mbar_init(bar(B_DSR), 256);
+    mbar_init(bar(B_DQF), 1);
+    mbar_init(bar(B_DQE), 128);
+    mbar_init(bar(B_ACC), 1);
+    mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -129,215 +122,193 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
+    if (DQ) asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer
-      mbar_expect_tx(bar(P_KV), 2 * C::KV_BYTES);
+      mbar_expect_tx(bar(B_KV), 2 * C::KV_BYTES);
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
-        tma_load_3d(sb + C::K_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(P_KV));
-        tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(P_KV));
+        tma_load_3d(sb + C::K_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(B_KV));
+        tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(B_KV));
       }
-      int last_q[C::QST], last_g[C::GST];
-      for (int s = 0; s < C::QST; ++s) last_q[s] = -1;
-      for (int s = 0; s < C::GST; ++s) last_g[s] = -1;
+      int last[C::STG] = {-1, -1};
       for (int u = 0; u < cnt; ++u) {
+        const int s = u % C::STG;
         const int q0 = (i_start + u) * C::BM;
-        const int qs = u % C::QST, gs = u % C::GST;
-        if (!mbar_wait(bar(P_QE + qs), ((u / C::QST) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+        if (!mbar_wait(bar(B_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
           break;
-        const uint32_t qa = sb + C::Q_OFF + qs * C::QSLOT;
-        mbar_expect_tx(bar(P_QF + qs), C::QT_BYTES + 2 * C::BM * 4);
+        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
+        mbar_expect_tx(bar(B_QF + s), 2 * C::QT_BYTES + 2 * C::BM * 4);
 #pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(qa + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(P_QF + qs));
-        bulk_load(qa + C::QT_BYTES, LSE2 + (size_t)bh * n_pad + q0, C::BM * 4, bar(P_QF + qs));
-        bulk_load(qa + C::QT_BYTES + 512, Dv + (size_t)bh * n_pad + q0, C::BM * 4, bar(P_QF + qs));
-        last_q[qs] = u;
-        if (!mbar_wait(bar(P_GE + gs), ((u / C::GST) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
-          break;
-        const uint32_t ga = sb + C::G_OFF + gs * C::QT_BYTES;
-        mbar_expect_tx(bar(P_GF + gs), C::QT_BYTES);
-#pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(ga + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(P_GF + gs));
-        last_g[gs] = u;
+        for (int kb = 0; kb < C::NKB; ++kb) {
+          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(B_QF + s));
+          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(B_QF + s));
+        }
+        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bh * n_pad + q0, C::BM * 4, bar(B_QF + s));
+        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bh * n_pad + q0, C::BM * 4,
+                  bar(B_QF + s));
+        if (s == 0) last[0] = u; else last[1] = u;
       }
-      if (*abort_flag) {   // let issued copies land before the CTA may exit
+      if (*abort_flag) {
         volatile int no_abort = 0;
-        mbar_wait(bar(P_KV), 0, &no_abort, ctl, SITE_BWD_KV);
-        for (int s = 0; s < C::QST; ++s)
-          if (last_q[s] >= 0)
-            mbar_wait(bar(P_QF + s), (last_q[s] / C::QST) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
-        for (int s = 0; s < C::GST; ++s)
-          if (last_g[s] >= 0)
-            mbar_wait(bar(P_GF + s), (last_g[s] / C::GST) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+        mbar_wait(bar(B_KV), 0, &no_abort, ctl, SITE_BWD_KV);
+        if (last[0] >= 0) mbar_wait(bar(B_QF), (last[0] / 2) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+        if (last[1] >= 0) mbar_wait(bar(B_QF + 1), (last[1] / 2) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V and Q/dO K-major
+      constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
-      constexpr uint32_t id_dq = idesc_bf16(128, C::BM, true, true);    // both MN-major
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS, K both MN-major
       const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
-      auto qaddr = [&](int u) { return sb + C::Q_OFF + (u % C::QST) * C::QSLOT; };
-      auto gaddr = [&](int u) { return sb + C::G_OFF + (u % C::GST) * C::QT_BYTES; };
-      // S^T(u) = K Q(u)^T into slot u & 1
-      auto issue_s = [&](int u) -> bool {
-        if (!mbar_wait(bar(P_QF + u % C::QST), (u / C::QST) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
+      auto stage = [&](int u) { return sb + C::ST_OFF + (u % C::STG) * C::STAGE; };
+      auto issue_s = [&](int u) -> bool {   // S^T(u) = K Q(u)^T
+        if (!mbar_wait(bar(B_QF + u % C::STG), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
           return false;
         tc_fence_after();
-        const uint32_t qa = qaddr(u);
+        const uint32_t qa = stage(u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::S_COL + (u & 1) * C::BM,
+          mma_ss(tmem + C::S_COL,
                  sdesc_sw128(ka + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(qa + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-        tc_commit(bar(P_SF + (u & 1)));
+        tc_commit(bar(B_SF));
         return true;
       };
-      // dP^T(u) = V dO(u)^T
-      auto issue_dp = [&](int u) -> bool {
-        if (!mbar_wait(bar(P_GF + u % C::GST), (u / C::GST) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
-          return false;
-        tc_fence_after();
-        const uint32_t ga = gaddr(u);
+      auto issue_dp = [&](int u) {          // dP^T(u) = V dO(u)^T  (stage already full)
+        const uint32_t ga = stage(u) + C::QT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::DP_COL,
                  sdesc_sw128(va + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(ga + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-        tc_commit(bar(P_DPF));
-        return true;
+        tc_commit(bar(B_DPF));
       };
-      bool ok = mbar_wait(bar(P_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
-      if (ok && cnt > 1) ok = issue_s(1);
+      if (ok) issue_dp(0);
       for (int u = 0; ok && u < cnt; ++u) {
-        const int b = u & 1;
-        const uint32_t qa = qaddr(u), ga = gaddr(u);
-        const uint32_t dsa = sb + C::DS_OFF + b * C::DS_BYTES;
-        // dV += P^T dO(u): P^T from TMEM slot b, where compute half h wrote
-        // queries [32h, 32h+32) packed into columns [32h, 32h+16)
-        if (!(ok = mbar_wait(bar(P_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
+        const uint32_t qa = stage(u), ga = qa + C::QT_BYTES;
+        // dV += P^T dO(u): P^T in the S columns, half h at [64h, 64h+32)
+        if (!(ok = mbar_wait(bar(B_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + b * C::BM + acol,
+          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
                  sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
         }
-        // dP^T(u+1) once the compute warps have read dP^T(u)
+        tc_commit(bar(B_DVD));
         if (u + 1 < cnt) {
-          if (!(ok = mbar_wait(bar(P_DPE), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE))) break;
-          if (!(ok = issue_dp(u + 1))) break;
+          if (!(ok = issue_s(u + 1))) break;
         }
-        if (!(ok = mbar_wait(bar(P_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        if (!(ok = mbar_wait(bar(B_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
-        // dK += dS^T Q(u)   (dS^T in smem, K-major over the 64 queries)
+        // dK += dS^T Q(u): dS^T [128 keys][128 queries] in the dO buffer, K-major
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ss(tmem + C::DK_COL, sdesc_sw128(dsa + kk * 32, 16, 1024),
+          mma_ss(tmem + C::DK_COL,
+                 sdesc_sw128(ga + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
         if (DQ) {
-          if (u >= 1) {
-            if (!(ok = mbar_wait(bar(P_DQE), (u - 1) & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
-            tc_fence_after();
-          }
-          // dQ^T(u) = K^T dS^T   (M = d, N = 64 queries, contraction over the 128 keys)
+          // dQ(u) = dS K into the dP^T columns (read by the compute warps already)
 #pragma unroll
           for (int kk = 0; kk < C::BNK / 16; ++kk)
-            mma_ss(tmem + C::DQ_COL, sdesc_sw128(ka + kk * 2048, C::BNK * 128, 1024),
-                   sdesc_sw128(dsa + kk * 2048, C::BNK * 128, 1024), id_dq, kk > 0);
-          tc_commit(bar(P_DQF));
+            mma_ss(tmem + C::DP_COL, sdesc_sw128(ga + kk * 2048, C::BNK * 128, 1024),
+                   sdesc_sw128(ka + kk * 2048, C::BNK * 128, 1024), id_dq, kk > 0);
+          tc_commit(bar(B_DQF));
         }
-        tc_commit(bar(P_QE + u % C::QST));
-        tc_commit(bar(P_GE + u % C::GST));
-        tc_commit(bar(P_DSE + b));
-        if (u + 2 < cnt) {
-          if (!(ok = issue_s(u + 2))) break;
+        tc_commit(bar(B_QE + u % C::STG));
+        if (u + 1 < cnt) {
+          if (DQ) {
+            if (!(ok = mbar_wait(bar(B_DQE), u & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
+            tc_fence_after();
+          }
+          issue_dp(u + 1);   // the stage of u + 1 is full: S(u+1) waited for it
         }
       }
-      tc_commit(bar(P_ACC));
+      tc_commit(bar(B_ACC));
       if (*abort_flag) {
-        tc_commit(bar(P_DRAIN));
+        tc_commit(bar(B_DRAIN));
         volatile int no_abort = 0;
-        mbar_wait(bar(P_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+        mbar_wait(bar(B_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
       }
     }
     __syncwarp();
   } else if (warp < 12) {
     // ---------------------------------------------------------------- compute
     const int q = warp & 3, h = (warp - 4) >> 2;
-    const int r = q * 32 + lane;          // key row (TMEM lane)
+    const int r = q * 32 + lane;
     const int key = k0 + r;
-    constexpr int NC = 32;                // queries of this thread: [32h, 32h+32)
+    constexpr int NC = 64;                 // queries [64h, 64h+64)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
     for (int u = 0; u < cnt; ++u) {
-      const int b = u & 1;
+      const int s = u % C::STG;
       const int q0 = (i_start + u) * C::BM;
-      const uint8_t* qp = smem + C::Q_OFF + (u % C::QST) * C::QSLOT;
-      const float* lse2 = reinterpret_cast<const float*>(qp + C::QT_BYTES) + h * NC;
-      const float* dd = reinterpret_cast<const float*>(qp + C::QT_BYTES + 512) + h * NC;
-      const uint32_t s_addr = tmem + lane_off + C::S_COL + b * C::BM + h * NC;
-      ok = mbar_wait(bar(P_QF + u % C::QST), (u / C::QST) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
-      ok = ok && mbar_wait(bar(P_SF + b), (u >> 1) & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+      uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
+      const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
+      const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
+      ok = mbar_wait(bar(B_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+      ok = ok && mbar_wait(bar(B_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const bool masked = causal && (k0 + C::BNK - 1 > q0);
       const int qbase = q0 + h * NC;
       float p[NC];
-      {
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(s_addr, rr);
+        tmem_ld32(s_addr + c0, rr);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[i]));
-          if (masked && key > qbase + i) v = 0.f;
-          p[i] = v;
+          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
+          if (masked && key > qbase + c0 + i) v = 0.f;
+          p[c0 + i] = v;
         }
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-        tmem_st16(s_addr, pk);
-        tmem_st_wait();
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
+        tmem_st16(s_addr + c0 / 2, pk);
       }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(P_PR));
-      ok = mbar_wait(bar(P_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+      mbar_arrive(bar(B_PR));
+      ok = mbar_wait(bar(B_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t ds[16];
-      {
+      uint32_t ds[NC / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(dp_addr, rr);
+        tmem_ld32(dp_addr + c0, rr);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(bar(P_DPE));        // the dP^T columns may be overwritten
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          ds[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(rr[2 * i]) - dd[2 * i]),
-                              p[2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[2 * i + 1]));
+          ds[c0 / 2 + i] =
+              pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
+                          p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
       }
-      if (u >= 2) {
-        ok = mbar_wait(bar(P_DSE + b), ((u >> 1) - 1) & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      // dS^T row of key r: [128 keys][64 queries] bf16, 128-byte swizzle;
-      // this half's 32 queries are chunks 4h .. 4h+3
-      uint8_t* dsb = smem + C::DS_OFF + b * C::DS_BYTES;
+      tc_fence_before();
+      // dS^T goes over dO(u), which dV(u) must have finished reading
+      ok = mbar_wait(bar(B_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      uint8_t* rowp = stp + C::QT_BYTES + h * (C::BNK * 128);   // query block h, key row r
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(dsb + sw128_offset(r, h * 4 + c)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
             make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
       fence_proxy_async_smem();
-      mbar_arrive(bar(P_DSR));
+      mbar_arrive(bar(B_DSR));
     }
-    // ---- epilogue: half 0 writes dV, half 1 writes dK (scaled)
     if (ok) {
-      ok = mbar_wait(bar(P_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
+      ok = mbar_wait(bar(B_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -355,33 +326,44 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else if (DQ) {
     // ---------------------------------------------------------------- dQ warpgroup
+    // Pulls the whole 128 x 128 fp32 dQ tile out of TMEM (thread = query row),
+    // releases the columns at once, then adds the tile into the accumulator
+    // as four 128 x 32 boxes staged in shared memory (128-byte swizzle) and
+    // one TMA bulk reduce-add each.  Rows past n are clipped by the tensor map.
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
     const int q = warp & 3;
-    const int r = q * 32 + lane;          // d column (TMEM lane of dQ^T)
-    const int et = threadIdx.x - 384;     // 0..127 within this warpgroup
-    float* stage = reinterpret_cast<float*>(smem + C::QS_OFF);
+    const int r = q * 32 + lane;
+    const int et = threadIdx.x - 384;
+    const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::DP_COL;
+    uint8_t* stage = smem + C::QS_OFF;
     for (int u = 0; u < cnt; ++u) {
-      bool ok = mbar_wait(bar(P_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
+      bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::DQ_COL;
-      uint32_t a[32], c[32];
-      tmem_ld32(src, a);
-      tmem_ld32(src + 32, c);
+      uint32_t v[4][32];
+      tmem_ld32(src, v[0]);
+      tmem_ld32(src + 32, v[1]);
+      tmem_ld32(src + 64, v[2]);
+      tmem_ld32(src + 96, v[3]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bar(P_DQE));            // the dQ^T columns may be refilled
-      if (et == 0) bulk_wait_read_all();  // the previous reduce has read the stage
-      named_bar_sync(1, 128);
+      mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
+      const int q0 = (i_start + u) * C::BM;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        stage[i * D + r] = scale * __uint_as_float(a[i]);
-        stage[(32 + i) * D + r] = scale * __uint_as_float(c[i]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (et == 0) {
-        tma_reduce_add_3d(&tmdQ, smem_u32(stage), 0, (i_start + u) * C::BM, bh);
-        bulk_commit_group();
+      for (int c = 0; c < 4; ++c) {
+        if (et == 0) bulk_wait_read_all();
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(stage + sw128_offset(r, j)) =
+              make_float4(scale * __uint_as_float(v[c][4 * j]), scale * __uint_as_float(v[c][4 * j + 1]),
+                          scale * __uint_as_float(v[c][4 * j + 2]), scale * __uint_as_float(v[c][4 * j + 3]));
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, q0, bh);
+          bulk_commit_group();
+        }
       }
     }
     if (et == 0) bulk_wait_all();
@@ -394,9 +376,9 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
 template <bool DQ>
 int launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-           const float* Dv, float* dQacc, void* dK, void* dV, int BH, int n, int n_pad,
-           float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
-  using C = Kv128<DQ>;
+             const float* Dv, float* dQacc, void* dK, void* dV, int BH, int n, int n_pad,
+             float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+  using C = Kv128;
   CUtensorMap tq, tk, tv, tg, tdq;
   if (!make_tmap_bf16(&tq, Q, 128, n, BH, 64, C::BM) ||
       !make_tmap_bf16(&tk, K, 128, n, BH, 64, C::BNK) ||
@@ -404,7 +386,7 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
       !make_tmap_bf16(&tg, dO, 128, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   if (DQ) {
-    if (!make_tmap_f32(&tdq, dQacc, 128, n, BH, 128, C::BM)) return ATTN_ERR_CUDA;
+    if (!make_tmap_f32(&tdq, dQacc, 128, n, BH, 32, C::BM, true)) return ATTN_ERR_CUDA;
   } else {
     tdq = tq;   // not read
   }
@@ -413,10 +395,10 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
       cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, C::BNK), BH);
-  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv,
-                                           static_cast<__nv_bfloat16*>(dK),
-                                           static_cast<__nv_bfloat16*>(dV), n, n_pad, scale,
-                                           scale * 1.4426950408889634f, causal, ctl);
+  kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
+                                              static_cast<__nv_bfloat16*>(dK),
+                                              static_cast<__nv_bfloat16*>(dV), n, n_pad, scale,
+                                              scale * 1.4426950408889634f, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

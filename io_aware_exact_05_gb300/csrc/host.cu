@@ -44,7 +44,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, 
 }
 
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
-                   uint32_t box_x, uint32_t box_y) {
+                   uint32_t box_x, uint32_t box_y, bool sw128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {x, y, z};
@@ -52,7 +52,8 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
   const cuuint32_t box[3] = {box_x, box_y, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

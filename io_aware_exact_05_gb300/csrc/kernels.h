@@ -15,9 +15,10 @@ namespace attn {
 // 128-byte swizzle and zero fill outside the tensor.  box_x * 2 must be 128.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
                     uint32_t box_x, uint32_t box_y);
-// A 3-D fp32 tensor map over [z][y][x] with no swizzle (for reduce-add tiles).
+// A 3-D fp32 tensor map over [z][y][x] for reduce-add tiles; with sw128 the
+// shared-memory tile uses the 128-byte swizzle (box_x * 4 must then be 128).
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
-                   uint32_t box_x, uint32_t box_y);
+                   uint32_t box_x, uint32_t box_y, bool sw128 = false);
 
 KernelCtl default_ctl();
 
