@@ -137,7 +137,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    if (QT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (QT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer
       uint32_t qbytes = 0;
@@ -254,7 +254,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
-    if (QT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    if (QT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
     const int t = (warp >> 2) - 1;
     const int q = warp & 3;                       // TMEM lane quarter
     const int r = q * 32 + lane;
@@ -271,15 +271,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!ok) break;
       tc_fence_after();
       const uint32_t sa = tmem + lane_off + C::S_COL + slot * BN;
-      float s[BN];
+      // all BN columns of this row: issue every TMEM load, then wait once
+      uint32_t sr[BN];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(sa + c0, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(rr[i]);
-      }
+      for (int c0 = 0; c0 < BN; c0 += 32)
+        tmem_ld32(sa + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+      tmem_ld_wait();
+      reg_fence<BN>(sr);
+      float* s = reinterpret_cast<float*>(sr);
       const int col0 = j * BN;
       const bool need_mask = (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
       if (need_mask) {
@@ -288,13 +287,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int c = 0; c < BN; ++c)
           if (col0 + c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row maximum with eight independent chains
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_cand = mx * scale_log2;
       const float m_new = (m_cand > m + 8.0f) ? m_cand : m;
       const float alpha = ex2(m - m_new);   // 0 on the first tile (m = -inf)
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -303,11 +307,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2(fmaf(s[c0 + 2 * i], scale_log2, -m_new));
           const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale_log2, -m_new));
-          rs += p0 + p1;
+          rs8[(2 * i) & 7] += p0;
+          rs8[(2 * i + 1) & 7] += p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(pa + c0 / 2, pk);
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       tmem_st_wait();
       l = l * alpha + rs;
       // Wait for PV of tile j-1 every iteration: a parity wait is only
