@@ -40,13 +40,14 @@ template <int D, int BN, int QT>
 struct FwdCfg {
   static constexpr int BM = 128;
   static constexpr int NKB = D / 64;            // 64-wide (128 B) column boxes
-  static constexpr int KST = (D == 64) ? 3 : 2; // K and V ring depth
+  static constexpr int KSTK = 3;                 // K ring depth
+  static constexpr int KSTV = (D == 64) ? 3 : 2; // V ring depth
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + QT * Q_BYTES;
-  static constexpr uint32_t V_OFF = K_OFF + KST * KV_BYTES;
-  static constexpr uint32_t BAR_OFF = V_OFF + KST * KV_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + KSTK * KV_BYTES;
+  static constexpr uint32_t BAR_OFF = V_OFF + KSTV * KV_BYTES;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
   static constexpr int S_COL = 0;               // two S slots of BN columns
   static constexpr int O_COL = 2 * BN;          // QT accumulators of D columns
@@ -62,6 +63,18 @@ enum : int { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 10, B_SF = 13, B_PF =
 struct TileInfo {
   int last0, last1;   // last KV tile index each query tile needs (-1: none)
 };
+
+// Unit k -> (query tile t, KV tile j) in the issue order j-major, t-minor.
+// Tile 1 never needs fewer KV tiles than tile 0, so the order is: pairs
+// (0, j), (1, j) while both tiles need j, then tile 1 alone.
+struct Unit { int t, j; };
+template <int QT>
+__device__ __forceinline__ Unit unit_at(int k, const TileInfo& ti) {
+  if (QT == 1 || ti.last1 < 0) return {0, k};
+  const int pairs = ti.last0 + 1;
+  if (k < 2 * pairs) return {k & 1, k >> 1};
+  return {1, k - pairs};
+}
 
 __device__ __forceinline__ int unit_pos(int t, int j, const TileInfo& ti) {
   return min(j, ti.last0 + 1) + min(j, ti.last1 + 1) + ((t == 1 && j <= ti.last0) ? 1 : 0);
@@ -112,9 +125,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
-    for (int s = 0; s < C::KST; ++s) {
+    for (int s = 0; s < C::KSTK; ++s) {
       mbar_init(bar(B_KF + s), 1);
       mbar_init(bar(B_KE + s), 1);
+    }
+    for (int s = 0; s < C::KSTV; ++s) {
       mbar_init(bar(B_VF + s), 1);
       mbar_init(bar(B_VE + s), 1);
     }
@@ -139,7 +154,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp < 4) {
     if (QT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
     if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------ producer
+      // --------------------------------------------------- producer: Q, then K tiles
       uint32_t qbytes = 0;
       for (int t = 0; t < QT; ++t)
         if (row0 + t * C::BM < n) qbytes += C::Q_BYTES;
@@ -151,19 +166,34 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tma_load_3d(sb + C::Q_OFF + t * C::Q_BYTES + kb * (C::BM * 128), &tmQ, kb * 64,
                       row0 + t * C::BM, bh, bar(B_Q));
       }
-      int last_k[C::KST], last_v[C::KST];
-      for (int s = 0; s < C::KST; ++s) last_k[s] = last_v[s] = -1;
+      int last_k[C::KSTK];
+      for (int s = 0; s < C::KSTK; ++s) last_k[s] = -1;
       for (int j = 0; j <= jmax; ++j) {
-        const int s = j % C::KST;
-        const uint32_t ph = ((j / C::KST) & 1) ^ 1;
-        if (!mbar_wait(bar(B_KE + s), ph, abort_flag, ctl, SITE_FWD_KV_EMPTY)) break;
+        const int s = j % C::KSTK;
+        if (!mbar_wait(bar(B_KE + s), ((j / C::KSTK) & 1) ^ 1, abort_flag, ctl, SITE_FWD_KV_EMPTY))
+          break;
         mbar_expect_tx(bar(B_KF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
           tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, j * BN, bh,
                       bar(B_KF + s));
         last_k[s] = j;
-        if (!mbar_wait(bar(B_VE + s), ph, abort_flag, ctl, SITE_FWD_KV_EMPTY)) break;
+      }
+      if (*abort_flag) {   // let issued copies land before the CTA may exit
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_Q), 0, &no_abort, ctl, SITE_FWD_LOAD_Q);
+        for (int s = 0; s < C::KSTK; ++s)
+          if (last_k[s] >= 0)
+            mbar_wait(bar(B_KF + s), (last_k[s] / C::KSTK) & 1, &no_abort, ctl, SITE_FWD_K_FULL);
+      }
+    } else if (warp == 3 && lane == 0) {
+      // --------------------------------------------------- producer: V tiles
+      int last_v[C::KSTV];
+      for (int s = 0; s < C::KSTV; ++s) last_v[s] = -1;
+      for (int j = 0; j <= jmax; ++j) {
+        const int s = j % C::KSTV;
+        if (!mbar_wait(bar(B_VE + s), ((j / C::KSTV) & 1) ^ 1, abort_flag, ctl, SITE_FWD_KV_EMPTY))
+          break;
         mbar_expect_tx(bar(B_VF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
@@ -171,78 +201,71 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                       bar(B_VF + s));
         last_v[s] = j;
       }
-      if (*abort_flag) {   // let issued copies land before the CTA may exit
+      if (*abort_flag) {
         volatile int no_abort = 0;
-        mbar_wait(bar(B_Q), 0, &no_abort, ctl, SITE_FWD_LOAD_Q);
-        for (int s = 0; s < C::KST; ++s) {
-          if (last_k[s] >= 0)
-            mbar_wait(bar(B_KF + s), (last_k[s] / C::KST) & 1, &no_abort, ctl, SITE_FWD_K_FULL);
+        for (int s = 0; s < C::KSTV; ++s)
           if (last_v[s] >= 0)
-            mbar_wait(bar(B_VF + s), (last_v[s] / C::KST) & 1, &no_abort, ctl, SITE_FWD_V_FULL);
-        }
+            mbar_wait(bar(B_VF + s), (last_v[s] / C::KSTV) & 1, &no_abort, ctl, SITE_FWD_V_FULL);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
+      // Per-unit bookkeeping is kept to a few integer operations: the MMA
+      // queue is shallow, so scalar work between units shows up as idle
+      // tensor cycles.
       constexpr uint32_t idesc_s = idesc_bf16(C::BM, BN, false, false);   // Q, K both K-major
       constexpr uint32_t idesc_o = idesc_bf16(C::BM, D, false, true);     // P (TMEM), V MN-major
-      auto need = [&](int t, int j) { return j <= (t == 0 ? ti.last0 : ti.last1); };
-      int total = 0;
-      for (int t = 0; t < QT; ++t) total += (t == 0 ? ti.last0 : ti.last1) + 1;
-      // Cursor over the needed units (t, j), j-major / t-minor.
-      struct Cur { int t, j; };
-      auto advance = [&](Cur& c) {
-        do {
-          if (++c.t == QT) { c.t = 0; ++c.j; }
-        } while (c.j <= jmax && !need(c.t, c.j));
-      };
-      Cur cs{0, 0}, cp{0, 0};   // next unit to get S, next unit to get PV
-      if (!need(0, 0)) { advance(cs); advance(cp); }
-      auto first_user = [&](int t, int j) { return t == 0 || !need(0, j); };
-      auto last_user = [&](int t, int j) { return t == QT - 1 || !need(QT - 1, j); };
+      constexpr uint32_t HI = sdesc_hi(1024);
+      const int total = (ti.last0 + 1) + (ti.last1 + 1);
+      const uint32_t q_lo = sdesc_lo(sb + C::Q_OFF, 16), k_lo = sdesc_lo(sb + C::K_OFF, 16);
+      const uint32_t v_lo = sdesc_lo(sb + C::V_OFF, BN * 128);
+      auto first_user = [&](int t, int j) { return t == 0 || j > ti.last0; };
+      auto last_user = [&](int t, int j) { return QT == 1 || t == 1 || j > ti.last1; };
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      // S(k) = Q_t K_j^T into S slot k & 1
       auto issue_s = [&](int k) -> bool {
-        const int t = cs.t, j = cs.j;
-        advance(cs);
-        const int s = j % C::KST;
-        if (first_user(t, j)) {
-          if (!mbar_wait(bar(B_KF + s), (j / C::KST) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
+        const Unit u = unit_at<QT>(k, ti);
+        const int s = u.j % C::KSTK;
+        const uint32_t qb = q_lo + u.t * (C::Q_BYTES >> 4), kb = k_lo + s * (C::KV_BYTES >> 4);
+        if (first_user(u.t, u.j)) {
+          if (!mbar_wait(bar(B_KF + s), (u.j / C::KSTK) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
             return false;
         }
         tc_fence_after();
-        const uint32_t qa = sb + C::Q_OFF + t * C::Q_BYTES;
-        const uint32_t ka = sb + C::K_OFF + s * C::KV_BYTES;
-        const uint32_t dst = tmem + C::S_COL + (k & 1) * BN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(qa + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(ka + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(dst, a, b, idesc_s, kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {   // one 64-wide column box of Q and K per group
+          uint32_t alo[4], blo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            alo[i] = qb + b * (C::BM * 128 / 16) + 2 * i;
+            blo[i] = kb + b * (BN * 128 / 16) + 2 * i;
+          }
+          mma_ss_x4(tmem + C::S_COL + (k & 1) * BN, alo, HI, blo, HI, idesc_s, b > 0);
         }
         tc_commit(bar(B_SF + (k & 1)));
-        if (last_user(t, j)) tc_commit(bar(B_KE + s));
+        if (last_user(u.t, u.j)) tc_commit(bar(B_KE + s));
         return true;
       };
       if (ok && total > 0) ok = issue_s(0);
       if (ok && total > 1) ok = issue_s(1);
       for (int k = 0; ok && k < total; ++k) {
-        const int t = cp.t, j = cp.j;
-        advance(cp);
-        const int s = j % C::KST;
+        const Unit u = unit_at<QT>(k, ti);
+        const int s = u.j % C::KSTV;
+        const uint32_t vb = v_lo + s * (C::KV_BYTES >> 4);
+        const uint32_t pa = tmem + C::S_COL + (k & 1) * BN;   // P: bf16 pairs, BN/2 columns
         if (!mbar_wait(bar(B_PF + (k & 1)), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
-        if (first_user(t, j)) {
-          if (!mbar_wait(bar(B_VF + s), (j / C::KST) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
+        if (first_user(u.t, u.j)) {
+          if (!mbar_wait(bar(B_VF + s), (u.j / C::KSTV) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
         }
         tc_fence_after();
-        const uint32_t pa = tmem + C::S_COL + (k & 1) * BN;       // P: bf16 pairs, BN/2 columns
-        const uint32_t va = sb + C::V_OFF + s * C::KV_BYTES;
-        const uint32_t dst = tmem + C::O_COL + t * D;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(va + kk * 2048, BN * 128, 1024);
-          mma_ts(dst, pa + kk * 8, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int b = 0; b < BN / 64; ++b) {   // 64 keys (4 MMAs of K = 16) per group
+          uint32_t blo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) blo[i] = vb + (4 * b + i) * (2048 / 16);
+          mma_ts_x4(tmem + C::O_COL + u.t * D, pa + 32 * b, blo, HI, idesc_o, (u.j > 0 || b > 0));
         }
-        tc_commit(bar(B_OD + t));
-        if (last_user(t, j)) tc_commit(bar(B_VE + s));
+        tc_commit(bar(B_OD + u.t));
+        if (last_user(u.t, u.j)) tc_commit(bar(B_VE + s));
         if (k + 2 < total) ok = issue_s(k + 2);
       }
       if (*abort_flag) {

@@ -208,6 +208,53 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Four MMAs of one K-block group, issued back to back from one asm block so
+// no other instruction lands between them.  Descriptors are passed as 32-bit
+// halves: lo[i] (start address and leading offset, which vary per MMA) and hi
+// (stride offset, version and swizzle, shared).  The first MMA accumulates
+// iff acc != 0; the other three always accumulate.
+__device__ __forceinline__ void mma_ss_x4(uint32_t d, const uint32_t (&alo)[4], uint32_t ahi,
+                                          const uint32_t (&blo)[4], uint32_t bhi, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a0, a1, a2, a3, b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %12, 0;\n\tsetp.eq.b32 t, %12, %12;\n\t"
+      "mov.b64 a0, {%1, %9};\n\tmov.b64 a1, {%2, %9};\n\tmov.b64 a2, {%3, %9};\n\tmov.b64 a3, {%4, %9};\n\t"
+      "mov.b64 b0, {%5, %10};\n\tmov.b64 b1, {%6, %10};\n\tmov.b64 b2, {%7, %10};\n\tmov.b64 b3, {%8, %10};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b0, %11, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %11, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %11, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %11, t;\n\t}\n" ::"r"(d),
+      "r"(alo[0]), "r"(alo[1]), "r"(alo[2]), "r"(alo[3]), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]),
+      "r"(blo[3]), "r"(ahi), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Same with A read from tensor memory: A of MMA i starts at column a_tmem + 8 i
+// (sixteen bf16 values of K per MMA, two per 32-bit column).
+__device__ __forceinline__ void mma_ts_x4(uint32_t d, uint32_t a_tmem, const uint32_t (&blo)[4],
+                                          uint32_t bhi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 b0, b1, b2, b3;\n\t.reg .b32 x1, x2, x3;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 t, %7, %7;\n\t"
+      "mov.b64 b0, {%2, %6};\n\tmov.b64 b1, {%3, %6};\n\tmov.b64 b2, {%4, %6};\n\tmov.b64 b3, {%5, %6};\n\t"
+      "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %8, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], b1, %8, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], b2, %8, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),
+      "r"(a_tmem), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]), "r"(blo[3]), "r"(bhi), "r"(acc),
+      "r"(idesc)
+      : "memory");
+}
+// Low and high 32-bit halves of the 128-byte-swizzle shared-memory descriptor
+// (same fields as sdesc_sw128).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
 // Tensor memory <-> registers, shape 32x32b: thread t of the warp moves lane
 // (base lane + t), N consecutive 32-bit columns.
 #define ATTN_R8(a, o) "=r"(a[o + 0]), "=r"(a[o + 1]), "=r"(a[o + 2]), "=r"(a[o + 3]), \
