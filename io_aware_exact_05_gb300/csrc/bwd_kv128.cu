@@ -23,11 +23,16 @@
 // dP^T [384,512).  The dQ tile reuses the dP^T columns once the compute
 // warps have read dP^T, so S of the next tile is issued right after dV and
 // its exponentials overlap this tile's dK and dQ products.  dS^T is written
-// over the dO tile of its stage (after dV has consumed dO).  The dQ
-// warpgroup (given 176 registers by setmaxnreg) pulls the whole fp32 dQ tile
-// out of TMEM, releases the columns, and adds the tile into the global fp32
-// accumulator as four 128 x 32 boxes staged in shared memory (128-byte
-// swizzle), one TMA bulk reduce-add each.  Every wait is bounded (mbar_wait).
+// over the dO tile of its stage (after dV has consumed dO).  dQ is issued
+// before dK so that its drain overlaps the dK product.  The dQ warpgroup
+// (given 176 registers by setmaxnreg) pulls the whole fp32 dQ tile out of
+// TMEM and releases the columns; each 64-row half (two warps) then adds its
+// rows into the global fp32 accumulator as four 64 x 32 boxes staged in its
+// own 8 KB of shared memory (128-byte swizzle), one TMA bulk reduce-add
+// each, so two reduce-adds are in flight.  Shared-memory bandwidth, not the
+// tensor pipe, bounds this kernel: the SS products read 128 B/clk while
+// they run, and the tile loads, dS^T stores and dQ staging share the port.
+// Every wait is bounded (mbar_wait).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -60,7 +65,7 @@ struct Kv128 {
   static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024;      // Q, dO, LSE2 (+0), D (+512)
   static constexpr uint32_t K_OFF = 0, V_OFF = KV_BYTES;
   static constexpr uint32_t ST_OFF = 2 * KV_BYTES;
-  static constexpr uint32_t QS_OFF = ST_OFF + STG * STAGE;     // dQ staging: [128][32] fp32
+  static constexpr uint32_t QS_OFF = ST_OFF + STG * STAGE;     // dQ staging: 2 x [64][32] fp32
   static constexpr uint32_t QS_BYTES = BM * 32 * 4;             // 16 KB, 128-byte swizzle
   static constexpr uint32_t BAR_OFF = QS_OFF + QS_BYTES;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
@@ -160,43 +165,66 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS, K both MN-major
-      const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
-      auto stage = [&](int u) { return sb + C::ST_OFF + (u % C::STG) * C::STAGE; };
+      // Descriptors from precomputed 32-bit halves; each group of four MMAs is
+      // issued from one asm block (the MMA queue is shallow, so scalar work
+      // between MMAs costs tensor time).
+      constexpr uint32_t HI = sdesc_hi(1024);
+      const uint32_t k_km = sdesc_lo(sb + C::K_OFF, 16);              // K tile, K-major
+      const uint32_t v_km = sdesc_lo(sb + C::V_OFF, 16);              // V tile, K-major
+      const uint32_t k_mn = sdesc_lo(sb + C::K_OFF, C::BNK * 128);    // K tile, MN-major
+      const uint32_t st_km = sdesc_lo(sb + C::ST_OFF, 16);            // stage 0, K-major
+      const uint32_t st_mn = sdesc_lo(sb + C::ST_OFF, C::BM * 128);   // stage 0, MN-major
+      const uint32_t ds_mn = sdesc_lo(sb + C::ST_OFF, C::BNK * 128);  // dS (dO buffer), MN-major
+      constexpr uint32_t STG16 = C::STAGE >> 4, QT16 = C::QT_BYTES >> 4;
+      // K-major operand, 64-wide column box b of a tile with `rows` rows
+      auto km4 = [](uint32_t base, int rows, int b, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + b * (rows * 128 / 16) + 2 * i;
+      };
+      // MN-major operand, K slices 4g .. 4g+3 (16 rows = 2048 bytes each)
+      auto mn4 = [](uint32_t base, int g, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + (4 * g + i) * (2048 / 16);
+      };
       auto issue_s = [&](int u) -> bool {   // S^T(u) = K Q(u)^T
         if (!mbar_wait(bar(B_QF + u % C::STG), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
           return false;
         tc_fence_after();
-        const uint32_t qa = stage(u);
+        const uint32_t qb = st_km + (u % C::STG) * STG16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::S_COL,
-                 sdesc_sw128(ka + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(qa + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {
+          uint32_t alo[4], blo[4];
+          km4(k_km, C::BNK, b, alo);
+          km4(qb, C::BM, b, blo);
+          mma_ss_x4(tmem + C::S_COL, alo, HI, blo, HI, id_s, b > 0);
+        }
         tc_commit(bar(B_SF));
         return true;
       };
       auto issue_dp = [&](int u) {          // dP^T(u) = V dO(u)^T  (stage already full)
-        const uint32_t ga = stage(u) + C::QT_BYTES;
+        const uint32_t gb = st_km + (u % C::STG) * STG16 + QT16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::DP_COL,
-                 sdesc_sw128(va + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(ga + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {
+          uint32_t alo[4], blo[4];
+          km4(v_km, C::BNK, b, alo);
+          km4(gb, C::BM, b, blo);
+          mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_s, b > 0);
+        }
         tc_commit(bar(B_DPF));
       };
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (ok) ok = issue_s(0);
       if (ok) issue_dp(0);
       for (int u = 0; ok && u < cnt; ++u) {
-        const uint32_t qa = stage(u), ga = qa + C::QT_BYTES;
+        const uint32_t so = (u % C::STG) * STG16;
         // dV += P^T dO(u): P^T in the S columns, half h at [64h, 64h+32)
         if (!(ok = mbar_wait(bar(B_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
-                 sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+        for (int g = 0; g < C::BM / 64; ++g) {
+          uint32_t blo[4];
+          mn4(st_mn + so + QT16, g, blo);
+          mma_ts_x4(tmem + C::DV_COL, tmem + C::S_COL + 64 * g, blo, HI, id_acc, (u > 0 || g > 0));
         }
         tc_commit(bar(B_DVD));
         if (u + 1 < cnt) {
@@ -204,19 +232,25 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         if (!(ok = mbar_wait(bar(B_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
+        if (DQ) {
+          // dQ(u) = dS K into the dP^T columns (read by the compute warps already);
+          // first, so that the dQ warpgroup drains it while dK runs
+#pragma unroll
+          for (int g = 0; g < C::BNK / 64; ++g) {
+            uint32_t alo[4], blo[4];
+            mn4(ds_mn + so + QT16, g, alo);
+            mn4(k_mn, g, blo);
+            mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_dq, g > 0);
+          }
+          tc_commit(bar(B_DQF));
+        }
         // dK += dS^T Q(u): dS^T [128 keys][128 queries] in the dO buffer, K-major
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ss(tmem + C::DK_COL,
-                 sdesc_sw128(ga + (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
-        if (DQ) {
-          // dQ(u) = dS K into the dP^T columns (read by the compute warps already)
-#pragma unroll
-          for (int kk = 0; kk < C::BNK / 16; ++kk)
-            mma_ss(tmem + C::DP_COL, sdesc_sw128(ga + kk * 2048, C::BNK * 128, 1024),
-                   sdesc_sw128(ka + kk * 2048, C::BNK * 128, 1024), id_dq, kk > 0);
-          tc_commit(bar(B_DQF));
+        for (int b = 0; b < C::BM / 64; ++b) {
+          uint32_t alo[4], blo[4];
+          km4(st_km + so + QT16, C::BNK, b, alo);
+          mn4(st_mn + so, b, blo);
+          mma_ss_x4(tmem + C::DK_COL, alo, HI, blo, HI, id_acc, (u > 0 || b > 0));
         }
         tc_commit(bar(B_QE + u % C::STG));
         if (u + 1 < cnt) {
@@ -326,16 +360,19 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else if (DQ) {
     // ---------------------------------------------------------------- dQ warpgroup
-    // Pulls the whole 128 x 128 fp32 dQ tile out of TMEM (thread = query row),
-    // releases the columns at once, then adds the tile into the accumulator
-    // as four 128 x 32 boxes staged in shared memory (128-byte swizzle) and
-    // one TMA bulk reduce-add each.  Rows past n are clipped by the tensor map.
+    // Pulls the whole 128 x 128 fp32 dQ tile out of TMEM (thread = query row)
+    // and releases the columns at once.  Each half (warps 2h, 2h+1 of the
+    // group: rows [64h, 64h+64)) then adds its rows into the accumulator as
+    // four 64 x 32 boxes through its own staging buffer, with its own named
+    // barrier and bulk group, so the two halves keep two reduce-adds in
+    // flight.  Rows past n are clipped by the tensor map.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int et = threadIdx.x - 384;
+    const int half = q >> 1, hr = r - 64 * half;
+    const bool lead = (lane == 0) && (q & 1) == 0;
     const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::DP_COL;
-    uint8_t* stage = smem + C::QS_OFF;
+    uint8_t* stage = smem + C::QS_OFF + half * (C::QS_BYTES / 2);
     for (int u = 0; u < cnt; ++u) {
       bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -348,25 +385,25 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
-      const int q0 = (i_start + u) * C::BM;
+      const int row0 = (i_start + u) * C::BM + 64 * half;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if (et == 0) bulk_wait_read_all();
-        named_bar_sync(1, 128);
+        if (lead) bulk_wait_read_all();
+        named_bar_sync(1 + half, 64);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(stage + sw128_offset(r, j)) =
+          *reinterpret_cast<float4*>(stage + sw128_offset(hr, j)) =
               make_float4(scale * __uint_as_float(v[c][4 * j]), scale * __uint_as_float(v[c][4 * j + 1]),
                           scale * __uint_as_float(v[c][4 * j + 2]), scale * __uint_as_float(v[c][4 * j + 3]));
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (et == 0) {
-          tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, q0, bh);
+        named_bar_sync(1 + half, 64);
+        if (lead && row0 < n) {
+          tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, row0, bh);
           bulk_commit_group();
         }
       }
     }
-    if (et == 0) bulk_wait_all();
+    if (lead) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -386,7 +423,7 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
       !make_tmap_bf16(&tg, dO, 128, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   if (DQ) {
-    if (!make_tmap_f32(&tdq, dQacc, 128, n, BH, 32, C::BM, true)) return ATTN_ERR_CUDA;
+    if (!make_tmap_f32(&tdq, dQacc, 128, n, BH, 32, C::BM / 2, true)) return ATTN_ERR_CUDA;
   } else {
     tdq = tq;   // not read
   }
