@@ -94,7 +94,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int kt = blockIdx.x, bh = blockIdx.y;
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
@@ -160,8 +160,9 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (last[0] >= 0) mbar_wait(bar(B_QF), (last[0] / 2) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
         if (last[1] >= 0) mbar_wait(bar(B_QF + 1), (last[1] / 2) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp runs the loop; one elected lane issues each MMA/commit)
       constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS, K both MN-major
@@ -187,7 +188,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int i = 0; i < 4; ++i) lo[i] = base + (4 * g + i) * (2048 / 16);
       };
       auto issue_s = [&](int u) -> bool {   // S^T(u) = K Q(u)^T
-        if (!mbar_wait(bar(B_QF + u % C::STG), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
+        if (!mbar_wait_warp(bar(B_QF + u % C::STG), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))
           return false;
         tc_fence_after();
         const uint32_t qb = st_km + (u % C::STG) * STG16;
@@ -212,13 +213,13 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         tc_commit(bar(B_DPF));
       };
-      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      bool ok = mbar_wait_warp(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (ok) ok = issue_s(0);
       if (ok) issue_dp(0);
       for (int u = 0; ok && u < cnt; ++u) {
         const uint32_t so = (u % C::STG) * STG16;
         // dV += P^T dO(u): P^T in the S columns, half h at [64h, 64h+32)
-        if (!(ok = mbar_wait(bar(B_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
+        if (!(ok = mbar_wait_warp(bar(B_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
         tc_fence_after();
 #pragma unroll
         for (int g = 0; g < C::BM / 64; ++g) {
@@ -230,7 +231,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (u + 1 < cnt) {
           if (!(ok = issue_s(u + 1))) break;
         }
-        if (!(ok = mbar_wait(bar(B_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        if (!(ok = mbar_wait_warp(bar(B_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
         if (DQ) {
           // dQ(u) = dS K into the dP^T columns (read by the compute warps already);
@@ -255,17 +256,17 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_commit(bar(B_QE + u % C::STG));
         if (u + 1 < cnt) {
           if (DQ) {
-            if (!(ok = mbar_wait(bar(B_DQE), u & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
+            if (!(ok = mbar_wait_warp(bar(B_DQE), u & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
             tc_fence_after();
           }
           issue_dp(u + 1);   // the stage of u + 1 is full: S(u+1) waited for it
         }
       }
       tc_commit(bar(B_ACC));
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         tc_commit(bar(B_DRAIN));
         volatile int no_abort = 0;
-        mbar_wait(bar(B_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+        mbar_wait_warp(bar(B_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
       }
     }
     __syncwarp();

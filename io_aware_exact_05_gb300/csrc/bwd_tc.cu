@@ -102,7 +102,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int kt = blockIdx.x, bh = blockIdx.y, oh = blockIdx.z;   // oh: dK/dV column half (d=256)
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
@@ -171,20 +171,21 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (issued_last[s] >= 0)
             mbar_wait(bar(K_QF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
+      // (the whole warp runs the loop; one elected lane issues each MMA/commit)
       constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V K-major, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS MN-major, K MN-major
-      bool ok = mbar_wait(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
       for (int u = 0; ok && u < cnt; ++u) {
         const int s = u % C::STG;
         const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
         const uint32_t qa = st, ga = st + C::QT_BYTES;
-        if (!(ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
+        if (!(ok = mbar_wait_warp(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
         if (C::WITH_DQ && u > 0) {
-          if (!(ok = mbar_wait(bar(K_DQE), (u - 1) & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
+          if (!(ok = mbar_wait_warp(bar(K_DQE), (u - 1) & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
         }
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T  (contraction over d, 16 per instruction)
@@ -205,7 +206,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         tc_commit(bar(K_DPF));
         // dV += P^T dO   (contraction over the BM queries of this tile)
-        if (!(ok = mbar_wait(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
+        if (!(ok = mbar_wait_warp(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
         tc_fence_after();
         const uint32_t boff = oh * 2 * (C::BM * 128);   // first dO/Q column box of this half
 #pragma unroll
@@ -218,7 +219,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         if (C::DS_ALIAS) tc_commit(bar(K_DVD));
         // dK += dS^T Q ; dQ_i = dS K
-        if (!(ok = mbar_wait(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk) {
@@ -238,10 +239,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_commit(bar(K_QE + s));
       }
       tc_commit(bar(K_ACC));
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         tc_commit(bar(K_DRAIN));
         volatile int no_abort = 0;
-        mbar_wait(bar(K_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+        mbar_wait_warp(bar(K_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
       }
     }
     __syncwarp();
@@ -431,7 +432,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int ntile = gridDim.x;
   const int it = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
   const int bh = blockIdx.y;
@@ -494,15 +495,16 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
           if (issued_last[s] >= 0)
             mbar_wait(bar(Q_KF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_KV);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
+      // MMA issuer (the whole warp runs the loop; one elected lane issues)
       constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);
       constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);
-      bool ok = mbar_wait(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
+      bool ok = mbar_wait_warp(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
       const uint32_t qa = sb + C::Q_OFF, ga = sb + C::G_OFF;
       for (int j = 0; ok && j < cnt; ++j) {
         const int s = j % C::STG;
         const uint32_t ka = sb + C::ST_OFF + s * 2 * C::KV_BYTES, va = ka + C::KV_BYTES;
-        if (!(ok = mbar_wait(bar(Q_KF + s), (j / C::STG) & 1, abort_flag, ctl, SITE_BWD_KV))) break;
+        if (!(ok = mbar_wait_warp(bar(Q_KF + s), (j / C::STG) & 1, abort_flag, ctl, SITE_BWD_KV))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -520,7 +522,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                  id_s, kk > 0);
         }
         tc_commit(bar(Q_DPF));
-        if (!(ok = mbar_wait(bar(Q_DSR), j & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+        if (!(ok = mbar_wait_warp(bar(Q_DSR), j & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
@@ -532,10 +534,10 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         tc_commit(bar(Q_KE + s));
       }
       tc_commit(bar(Q_ACC));
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         tc_commit(bar(Q_DRAIN));
         volatile int no_abort = 0;
-        mbar_wait(bar(Q_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
+        mbar_wait_warp(bar(Q_DRAIN), 0, &no_abort, ctl, SITE_BWD_ACC_DONE);
       }
     }
     __syncwarp();

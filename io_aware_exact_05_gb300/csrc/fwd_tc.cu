@@ -104,7 +104,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   const int ntile = gridDim.x;
   const int cta = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
@@ -207,11 +207,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (last_v[s] >= 0)
             mbar_wait(bar(B_VF + s), (last_v[s] / C::KSTV) & 1, &no_abort, ctl, SITE_FWD_V_FULL);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      // Per-unit bookkeeping is kept to a few integer operations: the MMA
-      // queue is shallow, so scalar work between units shows up as idle
-      // tensor cycles.
+      // The whole warp runs this loop (one elected lane issues each MMA and
+      // commit), so every descriptor stays warp-uniform.  Per-unit
+      // bookkeeping is kept to a few integer operations: the MMA queue is
+      // shallow, so scalar work between units shows up as idle tensor cycles.
       constexpr uint32_t idesc_s = idesc_bf16(C::BM, BN, false, false);   // Q, K both K-major
       constexpr uint32_t idesc_o = idesc_bf16(C::BM, D, false, true);     // P (TMEM), V MN-major
       constexpr uint32_t HI = sdesc_hi(1024);
@@ -220,14 +221,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t v_lo = sdesc_lo(sb + C::V_OFF, BN * 128);
       auto first_user = [&](int t, int j) { return t == 0 || j > ti.last0; };
       auto last_user = [&](int t, int j) { return QT == 1 || t == 1 || j > ti.last1; };
-      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      bool ok = mbar_wait_warp(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
       // S(k) = Q_t K_j^T into S slot k & 1
       auto issue_s = [&](int k) -> bool {
         const Unit u = unit_at<QT>(k, ti);
         const int s = u.j % C::KSTK;
         const uint32_t qb = q_lo + u.t * (C::Q_BYTES >> 4), kb = k_lo + s * (C::KV_BYTES >> 4);
         if (first_user(u.t, u.j)) {
-          if (!mbar_wait(bar(B_KF + s), (u.j / C::KSTK) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
+          if (!mbar_wait_warp(bar(B_KF + s), (u.j / C::KSTK) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
             return false;
         }
         tc_fence_after();
@@ -252,9 +253,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int s = u.j % C::KSTV;
         const uint32_t vb = v_lo + s * (C::KV_BYTES >> 4);
         const uint32_t pa = tmem + C::S_COL + (k & 1) * BN;   // P: bf16 pairs, BN/2 columns
-        if (!mbar_wait(bar(B_PF + (k & 1)), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
+        if (!mbar_wait_warp(bar(B_PF + (k & 1)), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
         if (first_user(u.t, u.j)) {
-          if (!mbar_wait(bar(B_VF + s), (u.j / C::KSTV) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
+          if (!mbar_wait_warp(bar(B_VF + s), (u.j / C::KSTV) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
         }
         tc_fence_after();
 #pragma unroll
@@ -268,10 +269,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (last_user(u.t, u.j)) tc_commit(bar(B_VE + s));
         if (k + 2 < total) ok = issue_s(k + 2);
       }
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         tc_commit(bar(B_DRAIN));
         volatile int no_abort = 0;
-        mbar_wait(bar(B_DRAIN), 0, &no_abort, ctl, SITE_FWD_O_DONE);
+        mbar_wait_warp(bar(B_DRAIN), 0, &no_abort, ctl, SITE_FWD_O_DONE);
       }
     }
     __syncwarp();

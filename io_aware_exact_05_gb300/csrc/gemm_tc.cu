@@ -64,7 +64,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 136);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN, b = blockIdx.z;
   const int nkb = (K + kBK - 1) / kBK;
 
@@ -118,12 +118,12 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
           mbar_wait(full(s), (issued_last[s] / kStages) & 1, &no_abort, c2, SITE_GEMM_FULL);
         }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (the whole warp runs the loop; one elected lane issues)
     constexpr uint32_t idesc = idesc_bf16(kBM, BN, !A_K, !B_K);
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % kStages;
-      if (!mbar_wait(full(s), (kb / kStages) & 1, abort_flag, ctl, SITE_GEMM_FULL)) break;
+      if (!mbar_wait_warp(full(s), (kb / kStages) & 1, abort_flag, ctl, SITE_GEMM_FULL)) break;
       tc_fence_after();
       const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
 #pragma unroll
@@ -134,10 +134,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
       tc_commit(empty(s));
     }
     tc_commit(acc_bar);
-    if (*abort_flag) {
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       tc_commit(drain_bar);
       volatile int no_abort = 0;
-      mbar_wait(drain_bar, 0, &no_abort, ctl, SITE_GEMM_ACC);
+      mbar_wait_warp(drain_bar, 0, &no_abort, ctl, SITE_GEMM_ACC);
     }
   }
   __syncwarp();

@@ -28,6 +28,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Warp index, broadcast from lane 0 so the compiler treats it (and what is
+// derived from it) as warp-uniform: an MMA issuer whose loop runs on the whole
+// warp keeps its descriptors in uniform registers.
+__device__ __forceinline__ int warp_id_uniform() {
+  return __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+}
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(
@@ -64,16 +71,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, acquiring at cluster scope: for barriers that threads of the peer CTA
+// arrive on (their writes before the arrive are visible after the wait).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait.  Returns true when the phase with `parity` completed.  After
 // `timeout_ns` of polling, or as soon as another thread of the CTA raised
 // `*abort`, it records ATTN_ERR_DEVICE_TIMEOUT (first error wins) with the
 // wait site, raises `*abort` and returns false: callers then leave their loop.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          const KernelCtl& ctl, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile int* abort,
+                                            const KernelCtl& ctl, int site) {
+  auto poll = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((spin & 255u) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > ctl.timeout_ns) {
@@ -83,6 +108,52 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          const KernelCtl& ctl, int site) {
+  return mbar_wait_t<false>(bar, parity, abort, ctl, site);
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, const KernelCtl& ctl,
+                                                  int site) {
+  return mbar_wait_t<true>(bar, parity, abort, ctl, site);
+}
+
+// Whole-warp forms (every lane waits; the result is the same on all lanes):
+// for loops that a whole warp runs, such as an MMA issuer.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               const KernelCtl& ctl, int site) {
+  return __all_sync(0xffffffffu, mbar_wait_t<false>(bar, parity, abort, ctl, site));
+}
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity,
+                                                       volatile int* abort, const KernelCtl& ctl,
+                                                       int site) {
+  return __all_sync(0xffffffffu, mbar_wait_t<true>(bar, parity, abort, ctl, site));
+}
+
+// ------------------------------------------------------------ CTA clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Barrier over every thread of every CTA of the cluster (release/acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Shared::cluster address of the location `addr` (a shared::cta address)
+// inside the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on an mbarrier given by its
+// shared::cluster address, possibly in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 // ------------------------------------------------------------------- TMA
@@ -154,16 +225,55 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(NCOLS)
                : "memory");
 }
+// CTA-pair forms: executed by one warp in each CTA of the pair; every
+// tcgen05 instruction of a kernel that uses them is of the pair form.
+template <int NCOLS>
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem) {
+  static_assert(NCOLS >= 32 && NCOLS <= 512 && (NCOLS & (NCOLS - 1)) == 0, "tmem cols");
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(NCOLS)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int NCOLS>
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(NCOLS)
+               : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
+// MMA issue and commit helpers below are called by a whole converged warp;
+// one lane, chosen by elect.sync, issues.  (Running the issue loop on the
+// whole warp keeps its values warp-uniform; a loop under `lane == 0` pays a
+// register-to-uniform move per descriptor and halves the MMA issue rate.)
+//
+// Arrive on `bar` once every tcgen05.mma issued so far by the elected lane is
+// done.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+// Pair forms: arrive on `bar` of this CTA, or on the barrier at the same
+// offset in every CTA of `mask`, once the pair MMAs issued so far are done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 
@@ -191,9 +301,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -201,9 +312,10 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -212,40 +324,57 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // no other instruction lands between them.  Descriptors are passed as 32-bit
 // halves: lo[i] (start address and leading offset, which vary per MMA) and hi
 // (stride offset, version and swizzle, shared).  The first MMA accumulates
-// iff acc != 0; the other three always accumulate.
-__device__ __forceinline__ void mma_ss_x4(uint32_t d, const uint32_t (&alo)[4], uint32_t ahi,
-                                          const uint32_t (&blo)[4], uint32_t bhi, uint32_t idesc,
-                                          uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 a0, a1, a2, a3, b0, b1, b2, b3;\n\t"
-      "setp.ne.b32 p, %12, 0;\n\tsetp.eq.b32 t, %12, %12;\n\t"
-      "mov.b64 a0, {%1, %9};\n\tmov.b64 a1, {%2, %9};\n\tmov.b64 a2, {%3, %9};\n\tmov.b64 a3, {%4, %9};\n\t"
-      "mov.b64 b0, {%5, %10};\n\tmov.b64 b1, {%6, %10};\n\tmov.b64 b2, {%7, %10};\n\tmov.b64 b3, {%8, %10};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b0, %11, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %11, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %11, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %11, t;\n\t}\n" ::"r"(d),
-      "r"(alo[0]), "r"(alo[1]), "r"(alo[2]), "r"(alo[3]), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]),
-      "r"(blo[3]), "r"(ahi), "r"(bhi), "r"(idesc), "r"(acc)
-      : "memory");
-}
+// iff acc != 0; the other three always accumulate.  The _pair forms issue
+// the CTA-pair MMA (M = 256: A rows and B columns split between the CTAs,
+// each CTA's half at the same shared-memory and tensor-memory addresses).
+#define ATTN_MMA_SS_X4(NAME, CG)                                                                 \
+  __device__ __forceinline__ void NAME(uint32_t d, const uint32_t(&alo)[4], uint32_t ahi,       \
+                                       const uint32_t(&blo)[4], uint32_t bhi, uint32_t idesc,   \
+                                       uint32_t acc) {                                          \
+    asm volatile(                                                                               \
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b64 a0, a1, a2, a3, b0, b1, b2, b3;\n\t"             \
+        "elect.sync _|e, 0xffffffff;\n\t"                                                        \
+        "setp.ne.b32 p, %12, 0;\n\tsetp.eq.b32 t, %12, %12;\n\t"                                \
+        "mov.b64 a0, {%1, %9};\n\tmov.b64 a1, {%2, %9};\n\t"                                    \
+        "mov.b64 a2, {%3, %9};\n\tmov.b64 a3, {%4, %9};\n\t"                                    \
+        "mov.b64 b0, {%5, %10};\n\tmov.b64 b1, {%6, %10};\n\t"                                  \
+        "mov.b64 b2, {%7, %10};\n\tmov.b64 b3, {%8, %10};\n\t"                                  \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a0, b0, %11, p;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a1, b1, %11, t;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a2, b2, %11, t;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a3, b3, %11, t;\n\t}\n" ::"r"(d),        \
+        "r"(alo[0]), "r"(alo[1]), "r"(alo[2]), "r"(alo[3]), "r"(blo[0]), "r"(blo[1]),           \
+        "r"(blo[2]), "r"(blo[3]), "r"(ahi), "r"(bhi), "r"(idesc), "r"(acc)                      \
+        : "memory");                                                                            \
+  }
+ATTN_MMA_SS_X4(mma_ss_x4, "1")
+ATTN_MMA_SS_X4(mma_pair_ss_x4, "2")
+#undef ATTN_MMA_SS_X4
+
 // Same with A read from tensor memory: A of MMA i starts at column a_tmem + 8 i
 // (sixteen bf16 values of K per MMA, two per 32-bit column).
-__device__ __forceinline__ void mma_ts_x4(uint32_t d, uint32_t a_tmem, const uint32_t (&blo)[4],
-                                          uint32_t bhi, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t.reg .b64 b0, b1, b2, b3;\n\t.reg .b32 x1, x2, x3;\n\t"
-      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 t, %7, %7;\n\t"
-      "mov.b64 b0, {%2, %6};\n\tmov.b64 b1, {%3, %6};\n\tmov.b64 b2, {%4, %6};\n\tmov.b64 b3, {%5, %6};\n\t"
-      "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %8, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], b1, %8, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], b2, %8, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),
-      "r"(a_tmem), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]), "r"(blo[3]), "r"(bhi), "r"(acc),
-      "r"(idesc)
-      : "memory");
-}
+#define ATTN_MMA_TS_X4(NAME, CG)                                                                 \
+  __device__ __forceinline__ void NAME(uint32_t d, uint32_t a_tmem, const uint32_t(&blo)[4],    \
+                                       uint32_t bhi, uint32_t idesc, uint32_t acc) {            \
+    asm volatile(                                                                               \
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b0, b1, b2, b3;\n\t.reg .b32 x1, x2, x3;\n\t"    \
+        "elect.sync _|e, 0xffffffff;\n\t"                                                        \
+        "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 t, %7, %7;\n\t"                                   \
+        "mov.b64 b0, {%2, %6};\n\tmov.b64 b1, {%3, %6};\n\t"                                    \
+        "mov.b64 b2, {%4, %6};\n\tmov.b64 b3, {%5, %6};\n\t"                                    \
+        "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"                  \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [%1], b0, %8, p;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x1], b1, %8, t;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x2], b2, %8, t;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),       \
+        "r"(a_tmem), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]), "r"(blo[3]), "r"(bhi), "r"(acc),    \
+        "r"(idesc)                                                                              \
+        : "memory");                                                                            \
+  }
+ATTN_MMA_TS_X4(mma_ts_x4, "1")
+ATTN_MMA_TS_X4(mma_pair_ts_x4, "2")
+#undef ATTN_MMA_TS_X4
+
 // Low and high 32-bit halves of the 128-byte-swizzle shared-memory descriptor
 // (same fields as sdesc_sw128).
 __host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
