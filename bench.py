@@ -116,10 +116,13 @@ def oracle_step(w, x, heads, n_sub=None):
     import oracle
 
     m = w.n if n_sub is None else n_sub
-    q, k, v, do = (x[n].reshape(w.B * w.H, w.n, w.d) for n in ("q", "k", "v", "do"))
+    q, do = (x[n].reshape(w.B * w.H, w.n, w.d) for n in ("q", "do"))
+    k, v = (x[n].reshape(w.B * w.kv_heads, w.n, w.d) for n in ("k", "v"))
+    g = w.H // w.kv_heads
     for h in heads:
-        oracle.attention_forward_head(q[h][:m], k[h][:m], v[h][:m], w.scale, w.causal)
-        oracle.attention_backward_head(q[h][:m], k[h][:m], v[h][:m], do[h][:m], w.scale,
+        hk = (h // w.H) * w.kv_heads + (h % w.H) // g   # key/value head of query head h
+        oracle.attention_forward_head(q[h][:m], k[hk][:m], v[hk][:m], w.scale, w.causal)
+        oracle.attention_backward_head(q[h][:m], k[hk][:m], v[hk][:m], do[h][:m], w.scale,
                                        w.causal)
 
 
@@ -175,8 +178,8 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-                       "causal": w.causal},
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "n": w.n,
+                       "d": w.d, "causal": w.causal},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -191,14 +194,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch():
+def traffic_per_launch(w):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel source and this workload."""
     p = os.path.join(ROOT, "profiles", "bwd_dkdv_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    if not d.get("workload", "").startswith(w.name + ":"):
         return None
     return d.get("dram_bytes_per_launch_full_workload")
 
@@ -223,14 +228,23 @@ def run_ours(args, w):
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    wsb = attn.attn_bwd_workspace_size(w.B, w.H, w.n, w.d, attn.ATTN_BF16, w.causal, mode)
+    wsb = attn.attn_bwd_gqa_workspace_size(w.B, w.H, w.kv_heads, w.n, w.d, attn.ATTN_BF16,
+                                           w.causal, mode)
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream()
     sc = w.scale
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
+    grouped = w.kv_heads != w.H
+
     def step(e=None):
         if e: e[0].record(st)
+        if grouped:   # the grouped backward is one call: timed as the dK/dV stage
+            attn.attn_fwd_gqa(q, k, v, o, lse, sc, w.causal, st)
+            if e: e[1].record(st); e[2].record(st)
+            attn.attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, sc, w.causal, mode, work, st)
+            if e: e[3].record(st); e[4].record(st)
+            return
         attn.attn_fwd(q, k, v, o, lse, sc, w.causal, st)
         if e: e[1].record(st)
         attn.attn_bwd_preprocess(o, do, lse, w.causal, mode, work, st)
@@ -318,15 +332,15 @@ def run_ours(args, w):
         kv_flops = fl["bwd"] if mode_used == "atomic" else fl["bwd"] * 8 // 10
         achieved = kv_flops / (kv_ms * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"])
-        tr = traffic_per_launch()
+        tr = traffic_per_launch(w)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "pct_of_peak": 100.0 * value / ws_n / peak,
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-                       "causal": w.causal, "dq_mode": args.mode,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "n": w.n,
+                       "d": w.d, "causal": w.causal, "dq_mode": args.mode,
                        "parallelism": "replicas x%d (heads independent)" % ws_n,
                        "l2": "inputs larger than L2: Q,K,V,dO = %.0f MB per GPU vs 126 MB L2"
                              % (h2d / 1e6)},

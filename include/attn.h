@@ -114,6 +114,37 @@ ATTN_API int attn_bwd(const void* Q, const void* K, const void* V, const void* O
              size_t workspace_bytes, void* stream);
 
 /*
+ * Grouped-query and multi-query attention ("Flash Attention: Revolutionizing
+ * Transformer Efficiency", section FlashAttention-2, item 3, names both as
+ * variants the method supports).  H query heads share H_kv key/value heads:
+ * query head h of batch b reads key/value head h / (H / H_kv) of batch b.
+ * H_kv must divide H; H_kv = H is attn_fwd / attn_bwd, H_kv = 1 is
+ * multi-query attention.
+ *   Q, O, dO, dQ : [B][H][n][d];  LSE : fp32 [B][H][n]
+ *   K, V, dK, dV : [B][H_kv][n][d]
+ * dK and dV of a key/value head are the sums over the query heads that read
+ * it: the key-tile kernel walks the query tiles of every head of the group,
+ * so the sums accumulate in tensor memory.  When B * H_kv * ceil(n / 128)
+ * key-tile CTAs would leave the GPU short of work, the group is split over
+ * several CTAs per key/value head that add their partial sums into fp32
+ * accumulators in the workspace (then converted); the workspace is
+ * attn_bwd_gqa_workspace_size(...) bytes (0 for invalid arguments).  Other
+ * arguments, layouts and errors as attn_fwd / attn_bwd, plus
+ * ATTN_ERR_INVALID_ARG when H_kv < 1 or H_kv does not divide H.  The
+ * materialise-P comparison path (attn_mat_*) has no grouped form.
+ */
+ATTN_API int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                          int B, int H, int H_kv, int n, int d, attn_dtype dtype, float scale,
+                          int causal, void* stream);
+ATTN_API size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int n, int d,
+                                            attn_dtype dtype, int causal, attn_dq_mode mode);
+ATTN_API int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                          int H, int H_kv, int n, int d, attn_dtype dtype, float scale,
+                          int causal, attn_dq_mode mode, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
  * The three stages attn_bwd runs, exported so a caller can schedule or time
  * them separately (same arguments and workspace as attn_bwd; call them in
  * this order on one stream, with the same dQ mode):

@@ -58,6 +58,12 @@ def lib():
             L.attn_bwd_workspace_size.restype = sz
             L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, i, vp, sz, vp]
             L.attn_bwd.restype = i
+            L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+            L.attn_fwd_gqa.restype = i
+            L.attn_bwd_gqa.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.attn_bwd_gqa.restype = i
+            L.attn_bwd_gqa_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+            L.attn_bwd_gqa_workspace_size.restype = sz
             L.attn_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
             L.attn_bwd_preprocess.restype = i
             L.attn_bwd_dkdv.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -135,6 +141,11 @@ def attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode=ATTN_DQ_AUTO):
     return int(lib().attn_bwd_workspace_size(B, H, n, d, dtype, int(bool(causal)), int(mode)))
 
 
+def attn_bwd_gqa_workspace_size(B, H, Hkv, n, d, dtype, causal, mode=ATTN_DQ_AUTO):
+    return int(lib().attn_bwd_gqa_workspace_size(B, H, Hkv, n, d, dtype, int(bool(causal)),
+                                                 int(mode)))
+
+
 def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AUTO,
              workspace=None, stream=None):
     B, H, n, d = _shape(Q)
@@ -147,6 +158,39 @@ def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AUTO,
                         int(bool(causal)), int(mode), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_bwd")
+
+
+def _kv_heads(Q, K):
+    B, H, n, d = _shape(Q)
+    Bk, Hkv, nk, dk = _shape(K)
+    if (Bk, nk, dk) != (B, n, d):
+        raise ValueError("K shape %s does not match Q shape %s" % (tuple(K.shape), tuple(Q.shape)))
+    return Hkv
+
+
+def attn_fwd_gqa(Q, K, V, O, LSE, scale, causal, stream=None):
+    """Grouped-query forward: K, V hold K.shape[1] heads shared by Q's heads."""
+    B, H, n, d = _shape(Q)
+    Hkv = _kv_heads(Q, K)
+    rc = lib().attn_fwd_gqa(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, Hkv, n, d,
+                            _dtype_code(Q), float(scale), int(bool(causal)), _stream(stream))
+    _check(rc, "attn_fwd_gqa")
+
+
+def attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AUTO,
+                 workspace=None, stream=None):
+    """Grouped-query backward: dK, dV ([B, H_kv, n, d]) sum over each group."""
+    B, H, n, d = _shape(Q)
+    Hkv = _kv_heads(Q, K)
+    dt = _dtype_code(Q)
+    need = attn_bwd_gqa_workspace_size(B, H, Hkv, n, d, dt, causal, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    rc = lib().attn_bwd_gqa(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                            _ptr(dK), _ptr(dV), B, H, Hkv, n, d, dt, float(scale),
+                            int(bool(causal)), int(mode), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_bwd_gqa")
 
 
 def _ws(workspace):
@@ -215,7 +259,10 @@ def forward(q, k, v, causal=False, scale=None, stream=None):
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    if k.shape[1] != H:   # grouped-query: fewer key/value heads than query heads
+        attn_fwd_gqa(q, k, v, o, lse, scale, causal, stream)
+    else:
+        attn_fwd(q, k, v, o, lse, scale, causal, stream)
     return o, lse
 
 
@@ -225,5 +272,8 @@ def backward(q, k, v, o, do, lse, causal=False, scale=None, mode=ATTN_DQ_AUTO,
     d = q.shape[-1]
     scale = (1.0 / d ** 0.5) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)
+    if k.shape[1] != q.shape[1]:
+        attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)
+    else:
+        attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)
     return dq, dk, dv

@@ -38,14 +38,34 @@ attn_dq_mode resolve_mode(int d, attn_dq_mode mode) {
   return mode;
 }
 
+// CTAs per key/value head for the bf16 key-tile kernel.  A group of query
+// heads shares one key/value head, so with few key/value heads the grid of
+// (key tiles x key/value heads) CTAs can be smaller than the GPU; the group is
+// then split over the smallest divisor of its size that brings the grid to
+// two CTAs per SM (152 SMs), each part adding into fp32 dK/dV accumulators.
+int group_split(int B, int H, int H_kv, int n, int d, attn_dtype dtype) {
+  const int group = H / H_kv;
+  if (dtype != ATTN_BF16 || group <= 1) return 1;
+  const long long ctas = (long long)((n + 127) / 128) * B * H_kv * (d == 256 ? 2 : 1);
+  int split = 1;
+  for (int c = 2; c <= group && ctas * split < 2 * 152; ++c)
+    if (group % c == 0) split = c;
+  return split;
+}
+
 struct BwdWorkspace {
   float* lse2;
   float* delta;
   float* dq_acc;
+  float* dk_acc;   // fp32 [B][H_kv][n][d] when gsplit > 1
+  float* dv_acc;
+  int gsplit;
   size_t bytes;
 };
 
-BwdWorkspace carve_bwd(void* base, int BH, int n, int d, attn_dtype dtype, attn_dq_mode mode) {
+BwdWorkspace carve_bwd(void* base, int B, int H, int H_kv, int n, int d, attn_dtype dtype,
+                       attn_dq_mode mode) {
+  const int BH = B * H;
   BwdWorkspace w{};
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -62,7 +82,15 @@ BwdWorkspace carve_bwd(void* base, int BH, int n, int d, attn_dtype dtype, attn_
       w.dq_acc = reinterpret_cast<float*>(p + off);
       off += round_up((size_t)BH * n * d * 4, kAlign);
     }
+    w.gsplit = group_split(B, H, H_kv, n, d, dtype);
+    if (w.gsplit > 1) {
+      const size_t kv_bytes = round_up((size_t)B * H_kv * n * d * 4, kAlign);
+      w.dk_acc = reinterpret_cast<float*>(p + off);
+      w.dv_acc = reinterpret_cast<float*>(p + off + kv_bytes);
+      off += 2 * kv_bytes;
+    }
   }
+  if (w.gsplit < 1) w.gsplit = 1;
   w.bytes = off;
   return w;
 }
@@ -98,24 +126,31 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; 
 
 extern "C" {
 
-int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-             int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
+int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int H_kv, int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
   if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return ATTN_ERR_INVALID_ARG;
   int rc = check_common(B, H, n, d, scale, causal);
   if (rc) return rc;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  const HeadMap hm{H, H / H_kv};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
   if (dtype == ATTN_F32) {
     if (d > 256) return ATTN_ERR_UNSUPPORTED;
     return cuda_rc(launch_fwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
-                                  static_cast<const float*>(V), static_cast<float*>(O), LSE, BH, n,
-                                  d, scale, causal, st));
+                                  static_cast<const float*>(V), static_cast<float*>(O), LSE, BH, hm,
+                                  n, d, scale, causal, st));
   }
   if (dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
-  return launch_fwd_tc(Q, K, V, O, LSE, BH, n, d, scale, causal, default_ctl(), st);
+  return launch_fwd_tc(Q, K, V, O, LSE, BH, hm, n, d, scale, causal, default_ctl(), st);
+}
+
+int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+             int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
+  return attn_fwd_gqa(Q, K, V, O, LSE, B, H, H, n, d, dtype, scale, causal, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int causal,
@@ -123,21 +158,31 @@ size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int
   if (check_common(B, H, n, d, 1.0f, causal) != ATTN_OK) return 0;
   if (dtype == ATTN_F32) {
     if (d > 256) return 0;
-    return carve_bwd(nullptr, B * H, n, d, dtype, mode).bytes;
+    return carve_bwd(nullptr, B, H, H, n, d, dtype, mode).bytes;
   }
   if (dtype != ATTN_BF16 || !bf16_head_dim(d)) return 0;
   const attn_dq_mode m = resolve_mode(d, mode);
   if (m == ATTN_DQ_ATOMIC && d > 128) return 0;
-  return carve_bwd(nullptr, B * H, n, d, dtype, m).bytes;
+  return carve_bwd(nullptr, B, H, H, n, d, dtype, m).bytes;
+}
+
+size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int n, int d, attn_dtype dtype,
+                                   int causal, attn_dq_mode mode) {
+  if (H_kv < 1 || H % H_kv != 0) return 0;
+  const size_t mha = attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode);
+  if (mha == 0) return 0;
+  const attn_dq_mode m = dtype == ATTN_BF16 ? resolve_mode(d, mode) : mode;
+  return carve_bwd(nullptr, B, H, H_kv, n, d, dtype, m).bytes;
 }
 
 // Shared checks of the backward stages.  On success fills the resolved mode
 // and the carved workspace.
-static int bwd_setup(int B, int H, int n, int d, attn_dtype dtype, float scale, int causal,
-                     attn_dq_mode mode, void* workspace, size_t workspace_bytes,
+static int bwd_setup(int B, int H, int H_kv, int n, int d, attn_dtype dtype, float scale,
+                     int causal, attn_dq_mode mode, void* workspace, size_t workspace_bytes,
                      attn_dq_mode* resolved, BwdWorkspace* w) {
   int rc = check_common(B, H, n, d, scale, causal);
   if (rc) return rc;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (mode != ATTN_DQ_AUTO && mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_PASS)
     return ATTN_ERR_INVALID_ARG;
   if (dtype == ATTN_F32) {
@@ -150,7 +195,7 @@ static int bwd_setup(int B, int H, int n, int d, attn_dtype dtype, float scale, 
   } else {
     return ATTN_ERR_INVALID_ARG;
   }
-  *w = carve_bwd(workspace, B * H, n, d, dtype, *resolved);
+  *w = carve_bwd(workspace, B, H, H_kv, n, d, dtype, *resolved);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) || workspace_bytes < w->bytes)
     return ATTN_ERR_WORKSPACE;
   return ATTN_OK;
@@ -168,7 +213,7 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, 
   if (!ptrs_ok({O, dO, LSE})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
-  int rc = bwd_setup(B, H, n, d, dtype, 1.0f, causal, mode, workspace, workspace_bytes, &m, &w);
+  int rc = bwd_setup(B, H, H, n, d, dtype, 1.0f, causal, mode, workspace, workspace_bytes, &m, &w);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_F32)
@@ -179,47 +224,78 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, 
                                    (int)round_up(n, 128), d, st));
 }
 
-int attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
-                  int B, int H, int n, int d, attn_dtype dtype, float scale, int causal,
-                  attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
+// dK, dV stage (and the atomic dQ shares) for H query heads sharing H_kv
+// key/value heads.
+static int bwd_dkdv_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                         void* dV, int B, int H, int H_kv, int n, int d, attn_dtype dtype,
+                         float scale, int causal, attn_dq_mode mode, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (!ptrs_ok({Q, K, V, dO, dK, dV})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
-  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,
+                     &w);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_F32)
     return ATTN_ERR_INVALID_ARG;   // the fp32 dK/dV kernel needs LSE: use attn_bwd
-  return launch_bwd_kv_tc(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr,
-                          dK, dV, B * H, n, (int)round_up(n, 128), d, scale, causal, default_ctl(),
-                          st);
+  const size_t kv_elems = (size_t)B * H_kv * n * d;
+  if (w.gsplit > 1) {   // split group: zero the fp32 dK/dV accumulators first
+    if (cudaMemsetAsync(w.dk_acc, 0, kv_elems * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(w.dv_acc, 0, kv_elems * 4, st) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  rc = launch_bwd_kv_tc(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr, dK,
+                        dV, w.dk_acc, w.dv_acc, B * H, HeadMap{H, H / H_kv}, w.gsplit, n,
+                        (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
+  if (rc || w.gsplit == 1) return rc;
+  rc = cuda_rc(launch_dq_convert(w.dk_acc, dK, kv_elems, st));
+  if (rc) return rc;
+  return cuda_rc(launch_dq_convert(w.dv_acc, dV, kv_elems, st));
 }
 
-int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
-                int H, int n, int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
-                void* workspace, size_t workspace_bytes, void* stream) {
+static int bwd_dq_impl(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
+                       int H, int H_kv, int n, int d, attn_dtype dtype, float scale, int causal,
+                       attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
   if (!ptrs_ok({dQ})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
-  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,
+                     &w);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;   // use attn_bwd
   if (m == ATTN_DQ_ATOMIC) return cuda_rc(launch_dq_convert(w.dq_acc, dQ, (size_t)B * H * n * d, st));
   if (!ptrs_ok({Q, K, V, dO})) return ATTN_ERR_INVALID_ARG;
-  return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, n, (int)round_up(n, 128), d,
-                         scale, causal, default_ctl(), st);
+  return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, HeadMap{H, H / H_kv}, n,
+                         (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
 }
 
-int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
-             attn_dtype dtype, float scale, int causal, attn_dq_mode mode, void* workspace,
-             size_t workspace_bytes, void* stream) {
+int attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                  int B, int H, int n, int d, attn_dtype dtype, float scale, int causal,
+                  attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_dkdv_impl(Q, K, V, dO, dK, dV, B, H, H, n, d, dtype, scale, causal, mode, workspace,
+                       workspace_bytes, stream);
+}
+
+int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
+                int H, int n, int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_dq_impl(Q, K, V, dO, dQ, B, H, H, n, d, dtype, scale, causal, mode, workspace,
+                     workspace_bytes, stream);
+}
+
+int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int n,
+                 int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!ptrs_ok({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
-  int rc = bwd_setup(B, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,
+                     &w);
   if (rc) return rc;
+  const HeadMap hm{H, H / H_kv};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
   if (dtype == ATTN_F32) {
@@ -228,19 +304,27 @@ int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const v
     rc = cuda_rc(launch_delta_f32(static_cast<const float*>(O), g, w.delta, BH, n, d, st));
     if (rc) return rc;
     rc = cuda_rc(launch_bwd_dkdv_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dK),
-                                     static_cast<float*>(dV), BH, n, d, scale, causal, st));
+                                     static_cast<float*>(dV), BH, hm, n, d, scale, causal, st));
     if (rc) return rc;
-    return cuda_rc(launch_bwd_dq_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dQ), BH, n, d,
-                                     scale, causal, st));
+    return cuda_rc(launch_bwd_dq_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dQ), BH, hm, n,
+                                     d, scale, causal, st));
   }
   rc = attn_bwd_preprocess(O, dO, LSE, B, H, n, d, dtype, causal, mode, workspace,
                            workspace_bytes, stream);
   if (rc) return rc;
-  rc = attn_bwd_dkdv(Q, K, V, dO, dK, dV, B, H, n, d, dtype, scale, causal, mode, workspace,
+  rc = bwd_dkdv_impl(Q, K, V, dO, dK, dV, B, H, H_kv, n, d, dtype, scale, causal, mode, workspace,
                      workspace_bytes, stream);
   if (rc) return rc;
-  return attn_bwd_dq(Q, K, V, dO, dQ, B, H, n, d, dtype, scale, causal, mode, workspace,
+  return bwd_dq_impl(Q, K, V, dO, dQ, B, H, H_kv, n, d, dtype, scale, causal, mode, workspace,
                      workspace_bytes, stream);
+}
+
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
+             attn_dtype dtype, float scale, int causal, attn_dq_mode mode, void* workspace,
+             size_t workspace_bytes, void* stream) {
+  return attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H, n, d, dtype, scale, causal, mode,
+                      workspace, workspace_bytes, stream);
 }
 
 size_t attn_mat_workspace_size(int B, int H, int n, int d) {

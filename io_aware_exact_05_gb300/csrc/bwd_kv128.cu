@@ -76,14 +76,17 @@ struct Kv128 {
 enum : int { B_KV = 0, B_QF = 1, B_QE = 3, B_SF = 5, B_DPF = 6, B_PR = 7, B_DVD = 8, B_DSR = 9,
              B_DQF = 10, B_DQE = 11, B_ACC = 12, B_DRAIN = 13 };
 
-template <bool DQ>
+// GROUPED: query heads share key/value heads (compiled separately so that the
+// one-head-per-head kernel keeps its simple loops).
+template <bool DQ, bool GROUPED>
 __global__ void __launch_bounds__(DQ ? 512 : 384, 1)
 bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const float* __restrict__ LSE2, const float* __restrict__ Dv,
                   float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
-                  __nv_bfloat16* __restrict__ dV, int n, int n_pad, float scale, float scale_log2,
-                  int causal, KernelCtl ctl) {
+                  __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
+                  float* __restrict__ dVacc, HeadMap hm, int gsplit, int n, int n_pad,
+                  float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = Kv128;
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
@@ -95,11 +98,19 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, bh = blockIdx.y;
+  const int kt = blockIdx.x, bh = blockIdx.y;   // bh: key/value head (K, V, dK, dV)
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
-  const int cnt = nq - i_start;
+  const int cnt = nq - i_start;   // query tiles per query head
+  // The query heads of this key/value head's group are split over gsplit
+  // CTAs (blockIdx.z); iteration u visits query tile i_start + u % cnt of
+  // query head qbase + u / cnt, so dK and dV accumulate over this CTA's part
+  // of the group (over the whole group when gsplit = 1).  Each role runs an
+  // outer loop over its heads and an inner loop over the query tiles.
+  const int gper = GROUPED ? hm.group / gsplit : 1;
+  const int qbase = GROUPED ? hm.q_of(bh, (int)blockIdx.z * gper) : bh;
+  const int total = gper * cnt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV), 1);
@@ -137,22 +148,28 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(B_KV));
       }
       int last[C::STG] = {-1, -1};
-      for (int u = 0; u < cnt; ++u) {
-        const int s = u % C::STG;
-        const int q0 = (i_start + u) * C::BM;
-        if (!mbar_wait(bar(B_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
-          break;
-        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
-        mbar_expect_tx(bar(B_QF + s), 2 * C::QT_BYTES + 2 * C::BM * 4);
+      bool go = true;
+      for (int gi = 0, u = 0; go && gi < gper; ++gi) {
+        const int bq = qbase + gi;
+        for (int ut = 0; ut < cnt; ++ut, ++u) {
+          const int s = u % C::STG;
+          const int q0 = (i_start + ut) * C::BM;
+          if (!mbar_wait(bar(B_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+            go = false;
+            break;
+          }
+          const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
+          mbar_expect_tx(bar(B_QF + s), 2 * C::QT_BYTES + 2 * C::BM * 4);
 #pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(B_QF + s));
-          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(B_QF + s));
+          for (int kb = 0; kb < C::NKB; ++kb) {
+            tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(B_QF + s));
+            tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(B_QF + s));
+          }
+          bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bq * n_pad + q0, C::BM * 4, bar(B_QF + s));
+          bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bq * n_pad + q0, C::BM * 4,
+                    bar(B_QF + s));
+          if (s == 0) last[0] = u; else last[1] = u;
         }
-        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bh * n_pad + q0, C::BM * 4, bar(B_QF + s));
-        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bh * n_pad + q0, C::BM * 4,
-                  bar(B_QF + s));
-        if (s == 0) last[0] = u; else last[1] = u;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
@@ -216,7 +233,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bool ok = mbar_wait_warp(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (ok) ok = issue_s(0);
       if (ok) issue_dp(0);
-      for (int u = 0; ok && u < cnt; ++u) {
+      for (int u = 0; ok && u < total; ++u) {
         const uint32_t so = (u % C::STG) * STG16;
         // dV += P^T dO(u): P^T in the S columns, half h at [64h, 64h+32)
         if (!(ok = mbar_wait_warp(bar(B_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
@@ -228,7 +245,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           mma_ts_x4(tmem + C::DV_COL, tmem + C::S_COL + 64 * g, blo, HI, id_acc, (u > 0 || g > 0));
         }
         tc_commit(bar(B_DVD));
-        if (u + 1 < cnt) {
+        if (u + 1 < total) {
           if (!(ok = issue_s(u + 1))) break;
         }
         if (!(ok = mbar_wait_warp(bar(B_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
@@ -254,7 +271,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           mma_ss_x4(tmem + C::DK_COL, alo, HI, blo, HI, id_acc, (u > 0 || b > 0));
         }
         tc_commit(bar(B_QE + u % C::STG));
-        if (u + 1 < cnt) {
+        if (u + 1 < total) {
           if (DQ) {
             if (!(ok = mbar_wait_warp(bar(B_DQE), u & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
             tc_fence_after();
@@ -280,67 +297,69 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
-    for (int u = 0; u < cnt; ++u) {
-      const int s = u % C::STG;
-      const int q0 = (i_start + u) * C::BM;
-      uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
-      const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
-      const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
-      ok = mbar_wait(bar(B_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
-      ok = ok && mbar_wait(bar(B_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      const bool masked = causal && (k0 + C::BNK - 1 > q0);
-      const int qbase = q0 + h * NC;
-      float p[NC];
+    for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
+      for (int ut = 0; ut < cnt; ++ut, ++u) {
+        const int s = u % C::STG;
+        const int q0 = (i_start + ut) * C::BM;
+        uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
+        const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
+        const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
+        ok = mbar_wait(bar(B_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+        ok = ok && mbar_wait(bar(B_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const bool masked = causal && (k0 + C::BNK - 1 > q0);
+        const int qbase = q0 + h * NC;
+        float p[NC];
 #pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(s_addr + c0, rr);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(s_addr + c0, rr);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
-          if (masked && key > qbase + c0 + i) v = 0.f;
-          p[c0 + i] = v;
+          for (int i = 0; i < 32; ++i) {
+            float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
+            if (masked && key > qbase + c0 + i) v = 0.f;
+            p[c0 + i] = v;
+          }
         }
+#pragma unroll
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
+          tmem_st16(s_addr + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_PR));
+        ok = mbar_wait(bar(B_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t ds[NC / 2];
+#pragma unroll
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(dp_addr + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            ds[c0 / 2 + i] =
+                pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
+                            p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
+        }
+        tc_fence_before();
+        // dS^T goes over dO(u), which dV(u) must have finished reading
+        ok = mbar_wait(bar(B_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint8_t* rowp = stp + C::QT_BYTES + h * (C::BNK * 128);   // query block h, key row r
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
+              make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_DSR));
       }
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
-        tmem_st16(s_addr + c0 / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_PR));
-      ok = mbar_wait(bar(B_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t ds[NC / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(dp_addr + c0, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          ds[c0 / 2 + i] =
-              pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
-                          p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
-      }
-      tc_fence_before();
-      // dS^T goes over dO(u), which dV(u) must have finished reading
-      ok = mbar_wait(bar(B_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      uint8_t* rowp = stp + C::QT_BYTES + h * (C::BNK * 128);   // query block h, key row r
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
-            make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(B_DSR));
     }
     if (ok) {
       ok = mbar_wait(bar(B_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
@@ -349,14 +368,25 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) {
       tc_fence_after();
       const uint32_t src = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      __nv_bfloat16* dst = (h == 0 ? dV : dK) + ((size_t)bh * n + key) * D;
       const float mul = h == 0 ? 1.f : scale;
+      const size_t row = (size_t)bh * n + key;
+      float* acc = GROUPED ? (h == 0 ? dVacc : dKacc) : nullptr;   // set when the group is split
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
-        if (key < n) store_row32_bf16(dst + c0, rr, mul);
+        if (key < n) {
+          if (acc) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(acc + row * D + c0 + i, mul * __uint_as_float(rr[i]),
+                         mul * __uint_as_float(rr[i + 1]), mul * __uint_as_float(rr[i + 2]),
+                         mul * __uint_as_float(rr[i + 3]));
+          } else {
+            store_row32_bf16((h == 0 ? dV : dK) + row * D + c0, rr, mul);
+          }
+        }
       }
     }
   } else if (DQ) {
@@ -374,33 +404,40 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const bool lead = (lane == 0) && (q & 1) == 0;
     const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::DP_COL;
     uint8_t* stage = smem + C::QS_OFF + half * (C::QS_BYTES / 2);
-    for (int u = 0; u < cnt; ++u) {
-      bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t v[4][32];
-      tmem_ld32(src, v[0]);
-      tmem_ld32(src + 32, v[1]);
-      tmem_ld32(src + 64, v[2]);
-      tmem_ld32(src + 96, v[3]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
-      const int row0 = (i_start + u) * C::BM + 64 * half;
+    bool go = true;
+    for (int gi = 0, u = 0; go && gi < gper; ++gi) {
+      const int bq = qbase + gi;
+      for (int ut = 0; ut < cnt; ++ut, ++u) {
+        bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
+        if (!__all_sync(0xffffffffu, ok)) {
+          go = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[4][32];
+        tmem_ld32(src, v[0]);
+        tmem_ld32(src + 32, v[1]);
+        tmem_ld32(src + 64, v[2]);
+        tmem_ld32(src + 96, v[3]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
+        const int row0 = (i_start + ut) * C::BM + 64 * half;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (lead) bulk_wait_read_all();
-        named_bar_sync(1 + half, 64);
+        for (int c = 0; c < 4; ++c) {
+          if (lead) bulk_wait_read_all();
+          named_bar_sync(1 + half, 64);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(stage + sw128_offset(hr, j)) =
-              make_float4(scale * __uint_as_float(v[c][4 * j]), scale * __uint_as_float(v[c][4 * j + 1]),
-                          scale * __uint_as_float(v[c][4 * j + 2]), scale * __uint_as_float(v[c][4 * j + 3]));
-        fence_proxy_async_smem();
-        named_bar_sync(1 + half, 64);
-        if (lead && row0 < n) {
-          tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, row0, bh);
-          bulk_commit_group();
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stage + sw128_offset(hr, j)) =
+                make_float4(scale * __uint_as_float(v[c][4 * j]), scale * __uint_as_float(v[c][4 * j + 1]),
+                            scale * __uint_as_float(v[c][4 * j + 2]), scale * __uint_as_float(v[c][4 * j + 3]));
+          fence_proxy_async_smem();
+          named_bar_sync(1 + half, 64);
+          if (lead && row0 < n) {
+            tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, row0, bq);
+            bulk_commit_group();
+          }
         }
       }
     }
@@ -412,15 +449,17 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 2) tmem_dealloc<512>(tmem);
 }
 
-template <bool DQ>
+template <bool DQ, bool GROUPED>
 int launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-             const float* Dv, float* dQacc, void* dK, void* dV, int BH, int n, int n_pad,
-             float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+             const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
+             int BH, const HeadMap& hm, int gsplit, int n, int n_pad, float scale, int causal,
+             const KernelCtl& ctl, cudaStream_t st) {
   using C = Kv128;
+  const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg, tdq;
   if (!make_tmap_bf16(&tq, Q, 128, n, BH, 64, C::BM) ||
-      !make_tmap_bf16(&tk, K, 128, n, BH, 64, C::BNK) ||
-      !make_tmap_bf16(&tv, V, 128, n, BH, 64, C::BNK) ||
+      !make_tmap_bf16(&tk, K, 128, n, BHkv, 64, C::BNK) ||
+      !make_tmap_bf16(&tv, V, 128, n, BHkv, 64, C::BNK) ||
       !make_tmap_bf16(&tg, dO, 128, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   if (DQ) {
@@ -428,14 +467,15 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
   } else {
     tdq = tq;   // not read
   }
-  auto kern = bwd_kv128_kernel<DQ>;
+  auto kern = bwd_kv128_kernel<DQ, GROUPED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::BNK), BH);
+  dim3 grid(ceil_div(n, C::BNK), BHkv, gsplit);
   kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
                                               static_cast<__nv_bfloat16*>(dK),
-                                              static_cast<__nv_bfloat16*>(dV), n, n_pad, scale,
+                                              static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
+                                              gsplit, n, n_pad, scale,
                                               scale * 1.4426950408889634f, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -444,11 +484,19 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
 
 int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
                         const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                        int BH, int n, int n_pad, float scale, int causal, const KernelCtl& ctl,
+                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
+                        int n_pad, float scale, int causal, const KernelCtl& ctl,
                         cudaStream_t st) {
-  if (dQacc)
-    return launch<true>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal, ctl, st);
-  return launch<false>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal, ctl, st);
+#define ATTN_KV128(DQQ, GRP)                                                                  \
+  return launch<DQQ, GRP>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit, n, \
+                          n_pad, scale, causal, ctl, st)
+  if (hm.group > 1) {
+    if (dQacc) ATTN_KV128(true, true);
+    ATTN_KV128(false, true);
+  }
+  if (dQacc) ATTN_KV128(true, false);
+  ATTN_KV128(false, false);
+#undef ATTN_KV128
 }
 
 }  // namespace attn

@@ -92,6 +92,7 @@ extern "C" int attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
   const size_t need = dtype == ATTN_BF16 ? 2 * stat_bytes : stat_bytes;
   if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;
 
+  const HeadMap hm{H, 1};
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch());
   if (!base) return ATTN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -103,10 +104,10 @@ extern "C" int attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
     if (launch_delta_f32(static_cast<const float*>(O), g, delta, (int)BH, n, d, st) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (launch_bwd_dkdv_f32(q, k, v, g, LSE, delta, static_cast<float*>(dK),
-                            static_cast<float*>(dV), (int)BH, n, d, scale, causal,
+                            static_cast<float*>(dV), (int)BH, hm, n, d, scale, causal,
                             st) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    return launch_bwd_dq_f32(q, k, v, g, LSE, delta, static_cast<float*>(dQ), (int)BH, n, d,
+    return launch_bwd_dq_f32(q, k, v, g, LSE, delta, static_cast<float*>(dQ), (int)BH, hm, n, d,
                              scale, causal, st) == cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;
@@ -118,9 +119,9 @@ extern "C" int attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
   if (launch_delta_bf16(O, dO, LSE, delta, lse2, nullptr, (int)BH, n, (int)n_pad, d, st) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  int rc = launch_bwd_kv_tc(Q, K, V, dO, lse2, delta, nullptr, dK, dV, (int)BH, n, (int)n_pad, d,
-                            scale, causal, ctl, st);
+  int rc = launch_bwd_kv_tc(Q, K, V, dO, lse2, delta, nullptr, dK, dV, nullptr, nullptr, (int)BH,
+                            hm, 1, n, (int)n_pad, d, scale, causal, ctl, st);
   if (rc) return rc;
-  return launch_bwd_q_tc(Q, K, V, dO, lse2, delta, dQ, (int)BH, n, (int)n_pad, d, scale, causal,
-                         ctl, st);
+  return launch_bwd_q_tc(Q, K, V, dO, lse2, delta, dQ, (int)BH, hm, n, (int)n_pad, d, scale,
+                         causal, ctl, st);
 }

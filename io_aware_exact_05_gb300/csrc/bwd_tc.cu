@@ -91,8 +91,9 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ LSE2, const float* __restrict__ Dv,
               float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
-              __nv_bfloat16* __restrict__ dV, int n, int n_pad, float scale, float scale_log2,
-              int causal, KernelCtl ctl) {
+              __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
+              float* __restrict__ dVacc, HeadMap hm, int gsplit, int n, int n_pad, float scale,
+              float scale_log2, int causal, KernelCtl ctl) {
   using C = KvCfg<D, DQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -103,11 +104,22 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, bh = blockIdx.y, oh = blockIdx.z;   // oh: dK/dV column half (d=256)
+  constexpr int NOH = D / C::DO;                  // dK/dV column parts (2 for d = 256)
+  const int kt = blockIdx.x;
+  const int oh = (int)blockIdx.z % NOH;          // oh: dK/dV column half (d = 256)
+  const int part = (int)blockIdx.z / NOH;        // part of the group (gsplit > 1)
+  const int bh = blockIdx.y;                     // key/value head (K, V, dK, dV)
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
-  const int cnt = nq - i_start;   // query tiles this CTA visits (>= 1)
+  const int cnt = nq - i_start;   // query tiles per query head (>= 1)
+  // The query heads of this key/value head's group are split over gsplit
+  // CTAs; iteration u visits query tile i_start + u % cnt of query head
+  // qbase + u / cnt, so dK and dV accumulate over this CTA's part of the
+  // group.  Each loop tracks (tile, head) incrementally.
+  const int gper = hm.group / gsplit;
+  const int qbase = hm.q_of(bh, part * gper);
+  const int total = gper * cnt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(K_KV), 1);
@@ -147,20 +159,21 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
       }
       int issued_last[2] = {-1, -1};
-      for (int u = 0; u < cnt; ++u) {
+      for (int u = 0, ut = 0, bq = qbase; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1,
+               bq += (ut == 0)) {
         const int s = u % C::STG;
-        const int q0 = (i_start + u) * C::BM;
+        const int q0 = (i_start + ut) * C::BM;
         if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
           break;
         const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
         mbar_expect_tx(bar(K_QF + s), 2 * C::QT_BYTES + 2 * C::STAT_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(K_QF + s));
-          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(K_QF + s));
+          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(K_QF + s));
+          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(K_QF + s));
         }
-        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bh * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
-        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bh * n_pad + q0, C::STAT_BYTES,
+        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bq * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
+        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bq * n_pad + q0, C::STAT_BYTES,
                   bar(K_QF + s));
         issued_last[s] = u;
       }
@@ -179,7 +192,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS MN-major, K MN-major
       bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
-      for (int u = 0; ok && u < cnt; ++u) {
+      for (int u = 0; ok && u < total; ++u) {
         const int s = u % C::STG;
         const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
         const uint32_t qa = st, ga = st + C::QT_BYTES;
@@ -256,9 +269,9 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
-    for (int u = 0; u < cnt; ++u) {
+    for (int u = 0, ut = 0; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1) {
       const int s = u % C::STG;
-      const int q0 = (i_start + u) * C::BM;
+      const int q0 = (i_start + ut) * C::BM;
       const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
       const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
       const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
@@ -341,14 +354,25 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (ok) {
       tc_fence_after();
       const uint32_t src = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      __nv_bfloat16* dst = (h == 0 ? dV : dK) + ((size_t)bh * n + key) * D + oh * C::DO;
+      const size_t off = ((size_t)bh * n + key) * D + oh * C::DO;
       const float mul = h == 0 ? 1.f : scale;
+      float* acc = (h == 0 ? dVacc : dKacc);   // set when the group is split over CTAs
 #pragma unroll 1
       for (int c0 = 0; c0 < C::DO; c0 += 32) {
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
-        if (key < n) store32_bf16(dst + c0, rr, mul);
+        if (key < n) {
+          if (acc) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(acc + off + c0 + i, mul * __uint_as_float(rr[i]),
+                         mul * __uint_as_float(rr[i + 1]), mul * __uint_as_float(rr[i + 2]),
+                         mul * __uint_as_float(rr[i + 3]));
+          } else {
+            store32_bf16((h == 0 ? dV : dK) + off + c0, rr, mul);
+          }
+        }
       }
     }
   } else {
@@ -356,12 +380,13 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int q = warp & 3;
     const int r = q * 32 + lane;     // query row within the tile
     const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::S_COL;
-    for (int u = 0; u < cnt; ++u) {
+    for (int u = 0, ut = 0, bq = qbase; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1,
+             bq += (ut == 0)) {
       bool ok = mbar_wait(bar(K_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int qrow = (i_start + u) * C::BM + r;
-      float* dst = dQacc + ((size_t)bh * n + qrow) * D;
+      const int qrow = (i_start + ut) * C::BM + r;
+      float* dst = dQacc + ((size_t)bq * n + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 64) {
         uint32_t a[32], b[32];
@@ -421,8 +446,8 @@ __global__ void __launch_bounds__(QCfg<D>::NTHREADS, 1)
 bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
              const float* __restrict__ LSE2, const float* __restrict__ Dv,
-             __nv_bfloat16* __restrict__ dQ, int n, int n_pad, float scale, float scale_log2,
-             int causal, KernelCtl ctl) {
+             __nv_bfloat16* __restrict__ dQ, HeadMap hm, int n, int n_pad, float scale,
+             float scale_log2, int causal, KernelCtl ctl) {
   using C = QCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -435,7 +460,8 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   const int ntile = gridDim.x;
   const int it = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.y;          // query head (Q, dO, dQ, LSE, D)
+  const int bkv = hm.kv_of(bh);       // key/value head (K, V)
   const int q0 = it * C::BM;
   const int nkv = (n + C::BN - 1) / C::BN;
   const int jend = causal ? min(nkv - 1, (q0 + C::BM - 1) / C::BN) : nkv - 1;
@@ -482,8 +508,8 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         mbar_expect_tx(bar(Q_KF + s), 2 * C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, j * C::BN, bh, bar(Q_KF + s));
-          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, j * C::BN, bh,
+          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, j * C::BN, bkv, bar(Q_KF + s));
+          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, j * C::BN, bkv,
                       bar(Q_KF + s));
         }
         issued_last[s] = j;
@@ -614,56 +640,69 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 
 template <int D, bool DQ>
 int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-              const float* Dv, float* dQacc, void* dK, void* dV, int BH, int n, int n_pad,
-              float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+                  const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
+                  int BH, const HeadMap& hm, int gsplit, int n, int n_pad, float scale, int causal,
+                  const KernelCtl& ctl, cudaStream_t st) {
   using C = KvCfg<D, DQ>;
+  const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
-  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, C::BNK) ||
-      !make_tmap_bf16(&tv, V, D, n, BH, 64, C::BNK) || !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) ||
+      !make_tmap_bf16(&tk, K, D, n, BHkv, 64, C::BNK) ||
+      !make_tmap_bf16(&tv, V, D, n, BHkv, 64, C::BNK) ||
+      !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   auto kern = bwd_kv_kernel<D, DQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::BNK), BH, D / C::DO);
+  dim3 grid(ceil_div(n, C::BNK), BHkv, (D / C::DO) * gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
                                            static_cast<__nv_bfloat16*>(dK),
-                                           static_cast<__nv_bfloat16*>(dV), n, n_pad, scale,
-                                           scale * 1.4426950408889634f, causal, ctl);
+                                           static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
+                                           gsplit, n, n_pad, scale, scale * 1.4426950408889634f,
+                                           causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D>
 int launch_q(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-             const float* Dv, void* dQ, int BH, int n, int n_pad, float scale, int causal,
-             const KernelCtl& ctl, cudaStream_t st) {
+             const float* Dv, void* dQ, int BH, const HeadMap& hm, int n, int n_pad, float scale,
+             int causal, const KernelCtl& ctl, cudaStream_t st) {
   using C = QCfg<D>;
+  const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
-  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, C::BN) ||
-      !make_tmap_bf16(&tv, V, D, n, BH, 64, C::BN) || !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) ||
+      !make_tmap_bf16(&tk, K, D, n, BHkv, 64, C::BN) ||
+      !make_tmap_bf16(&tv, V, D, n, BHkv, 64, C::BN) ||
+      !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   auto kern = bwd_q_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, C::BM), BH);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, static_cast<__nv_bfloat16*>(dQ),
-                                           n, n_pad, scale, scale * 1.4426950408889634f, causal, ctl);
+                                           hm, n, n_pad, scale, scale * 1.4426950408889634f, causal,
+                                           ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
-                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV, int BH,
-                     int n, int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
+                     int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
                      cudaStream_t st) {
-#define ATTN_KV(DD, DQQ) \
-  return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal, ctl, st)
+  if (gsplit < 1 || hm.group % gsplit != 0 || (gsplit > 1 && (!dKacc || !dVacc)))
+    return ATTN_ERR_INVALID_ARG;
+#define ATTN_KV(DD, DQQ)                                                                      \
+  return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm,    \
+                                gsplit, n, n_pad, scale, causal, ctl, st)
   const bool dq = dQacc != nullptr;
   switch (d) {
     case 64: if (dq) { ATTN_KV(64, true); } else { ATTN_KV(64, false); }
     case 128:
-      return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, n, n_pad, scale, causal,
-                                 ctl, st);
+      return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit,
+                                 n, n_pad, scale, causal, ctl, st);
     case 256: if (dq) return ATTN_ERR_UNSUPPORTED; ATTN_KV(256, false);
     default: return ATTN_ERR_UNSUPPORTED;
   }
@@ -671,12 +710,13 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
 }
 
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
-                    const float* LSE2, const float* Dv, void* dQ, int BH, int n, int n_pad, int d,
-                    float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm, int n,
+                    int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                    cudaStream_t st) {
   switch (d) {
-    case 64: return launch_q<64>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
-    case 128: return launch_q<128>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
-    case 256: return launch_q<256>(Q, K, V, dO, LSE2, Dv, dQ, BH, n, n_pad, scale, causal, ctl, st);
+    case 64: return launch_q<64>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
+    case 128: return launch_q<128>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
+    case 256: return launch_q<256>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
     default: return ATTN_ERR_UNSUPPORTED;
   }
 }

@@ -8,6 +8,21 @@
 
 namespace attn {
 
+// Query heads -> key/value heads (grouped-query attention, "Flash Attention:
+// Revolutionizing Transformer Efficiency", section FlashAttention-2, item 3):
+// query head h of batch b reads key/value head h / group of the same batch;
+// there are H / group key/value heads per batch (group = 1: one per query
+// head, group = H: a single shared one).  Indices are flat b * heads + h.
+struct HeadMap {
+  int H;       // query heads per batch
+  int group;   // query heads per key/value head (divides H)
+  __host__ __device__ int hkv() const { return H / group; }
+  __host__ __device__ int kv_of(int bh) const { return (bh / H) * (H / group) + (bh % H) / group; }
+  __host__ __device__ int q_of(int bkv, int i) const {
+    return (bkv / (H / group)) * H + (bkv % (H / group)) * group + i;
+  }
+};
+
 // Passed by value to every kernel that waits on a barrier.
 struct KernelCtl {
   int* err;              // device status word: [0] = first error code, [1] = site

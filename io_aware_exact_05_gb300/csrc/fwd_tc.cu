@@ -89,11 +89,14 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
     reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
-template <int D, int BN, int QT>
+// GROUPED: query heads share key/value heads (compiled separately so the
+// one-head-per-head kernel does no head arithmetic).
+template <int D, int BN, int QT, bool GROUPED>
 __global__ void __launch_bounds__(FwdCfg<D, BN, QT>::NTHREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-              float* __restrict__ LSE, int n, float scale_log2, int causal, KernelCtl ctl) {
+              float* __restrict__ LSE, HeadMap hm, int n, float scale_log2, int causal,
+              KernelCtl ctl) {
   using C = FwdCfg<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -105,7 +108,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.y;        // query head (Q, O, LSE)
+  const int bkv = GROUPED ? hm.kv_of(bh) : bh;   // key/value head (K, V)
   const int ntile = gridDim.x;
   const int cta = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
   const int row0 = cta * (QT * C::BM);
@@ -175,7 +179,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_expect_tx(bar(B_KF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, j * BN, bh,
+          tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, j * BN, bkv,
                       bar(B_KF + s));
         last_k[s] = j;
       }
@@ -197,7 +201,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_expect_tx(bar(B_VF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(sb + C::V_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmV, kb * 64, j * BN, bh,
+          tma_load_3d(sb + C::V_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmV, kb * 64, j * BN, bkv,
                       bar(B_VF + s));
         last_v[s] = j;
       }
@@ -397,32 +401,35 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 }
 
 template <int D, int BN, int QT>
-int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
-               float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
+               const HeadMap& hm, int n, float scale, int causal, const KernelCtl& ctl,
+               cudaStream_t st) {
   using C = FwdCfg<D, BN, QT>;
+  const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BH, 64, BN) ||
-      !make_tmap_bf16(&tv, V, D, n, BH, 64, BN))
+  if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BHkv, 64, BN) ||
+      !make_tmap_bf16(&tv, V, D, n, BHkv, 64, BN))
     return ATTN_ERR_CUDA;
-  auto kern = fwd_tc_kernel<D, BN, QT>;
+  auto kern = hm.group > 1 ? fwd_tc_kernel<D, BN, QT, true> : fwd_tc_kernel<D, BN, QT, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, QT * C::BM), BH);
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, n,
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, hm, n,
                                            scale_log2, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
-                  int d, float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
+                  const HeadMap& hm, int n, int d, float scale, int causal, const KernelCtl& ctl,
+                  cudaStream_t st) {
   switch (d) {
-    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
-    case 128: return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
-    case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, n, scale, causal, ctl, st);
+    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
+    case 128: return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
+    case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
     default: return ATTN_ERR_UNSUPPORTED;
   }
 }

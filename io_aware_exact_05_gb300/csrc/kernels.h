@@ -23,16 +23,20 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
 KernelCtl default_ctl();
 
 // ---- fp32 SIMT path --------------------------------------------------------
+// BH counts query heads (B * H); K, V (and dK, dV) hold BH / hm.group heads.
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
-                           int BH, int n, int d, float scale, int causal, cudaStream_t st);
+                           int BH, const HeadMap& hm, int n, int d, float scale, int causal,
+                           cudaStream_t st);
 cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH, int n, int d,
                              cudaStream_t st);
 cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, const float* dO,
                                 const float* LSE, const float* Dv, float* dK, float* dV, int BH,
-                                int n, int d, float scale, int causal, cudaStream_t st);
+                                const HeadMap& hm, int n, int d, float scale, int causal,
+                                cudaStream_t st);
 cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, const float* dO,
-                              const float* LSE, const float* Dv, float* dQ, int BH, int n, int d,
-                              float scale, int causal, cudaStream_t st);
+                              const float* LSE, const float* Dv, float* dQ, int BH,
+                              const HeadMap& hm, int n, int d, float scale, int causal,
+                              cudaStream_t st);
 
 // ---- bf16 helpers ------------------------------------------------------------
 cudaError_t launch_delta_bf16(const void* O, const void* dO, const float* LSE, float* Dv,
@@ -45,24 +49,33 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, in
                      bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
                      cudaStream_t st);
 
-int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int n,
-                  int d, float scale, int causal, const KernelCtl& ctl, cudaStream_t st);
+int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
+                  const HeadMap& hm, int n, int d, float scale, int causal, const KernelCtl& ctl,
+                  cudaStream_t st);
 
 // Key-tile backward: dK, dV (and, with dQacc != nullptr, atomic dQ shares).
+// One CTA per (key tile, key/value head, part of the group) walks the query
+// tiles of the query heads of its part, so dK and dV sum over them in tensor
+// memory.  gsplit = 1: one part, dK and dV stored as bf16.  gsplit > 1: each
+// part adds its sums into the fp32 accumulators dKacc, dVacc (zeroed by the
+// caller; dK already scaled), which the caller converts.
 int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
-                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV, int BH,
-                     int n, int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                     const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
+                     int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
                      cudaStream_t st);
 // Key-tile backward for d = 128, pipelined two query tiles deep (dQ shares
 // reduced into dQacc with TMA bulk reduce-add when dQacc != nullptr).
 int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
                         const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                        int BH, int n, int n_pad, float scale, int causal, const KernelCtl& ctl,
+                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
+                        int n_pad, float scale, int causal, const KernelCtl& ctl,
                         cudaStream_t st);
 // Query-tile backward: dQ with no atomics.
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
-                    const float* LSE2, const float* Dv, void* dQ, int BH, int n, int n_pad, int d,
-                    float scale, int causal, const KernelCtl& ctl, cudaStream_t st);
+                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm, int n,
+                    int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
+                    cudaStream_t st);
 
 // ---- materialise-P row kernels ----------------------------------------------------
 cudaError_t launch_mat_softmax(const float* S, void* P, float* LSE, int BH, int n, float scale,

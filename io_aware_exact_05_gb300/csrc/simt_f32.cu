@@ -29,14 +29,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
 fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                const float* __restrict__ V, float* __restrict__ O, float* __restrict__ LSE,
-               int n, int d, float scale, int causal) {
+               HeadMap hm, int n, int d, float scale, int causal) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const size_t bh = blockIdx.y;
+  const size_t bkv = hm.kv_of((int)bh);
   if (row >= n) return;
   const float* q = Q + (bh * n + row) * d;
-  const float* k = K + bh * n * d;
-  const float* v = V + bh * n * d;
+  const float* k = K + bkv * n * d;
+  const float* v = V + bkv * n * d;
   float qr[kMaxPerLane], acc[kMaxPerLane];
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
@@ -97,15 +98,16 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 bwd_dq_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                   const float* __restrict__ V, const float* __restrict__ dO,
                   const float* __restrict__ LSE, const float* __restrict__ Dv,
-                  float* __restrict__ dQ, int n, int d, float scale, int causal) {
+                  float* __restrict__ dQ, HeadMap hm, int n, int d, float scale, int causal) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const size_t bh = blockIdx.y;
+  const size_t bkv = hm.kv_of((int)bh);
   if (row >= n) return;
   const float* q = Q + (bh * n + row) * d;
   const float* g = dO + (bh * n + row) * d;
-  const float* k = K + bh * n * d;
-  const float* v = V + bh * n * d;
+  const float* k = K + bkv * n * d;
+  const float* v = V + bkv * n * d;
   const float lse = LSE[bh * n + row];
   const float Di = Dv[bh * n + row];
   float qr[kMaxPerLane], gr[kMaxPerLane], acc[kMaxPerLane];
@@ -147,21 +149,20 @@ bwd_dq_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
   }
 }
 
-// dV_j = sum_i p_ij dO_i ; dK_j = scale * sum_i dS_ij q_i  (one warp per key row)
+// dV_j = sum_i p_ij dO_i ; dK_j = scale * sum_i dS_ij q_i  (one warp per key row;
+// the sums run over every query head that reads this key/value head)
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
 bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                     const float* __restrict__ V, const float* __restrict__ dO,
                     const float* __restrict__ LSE, const float* __restrict__ Dv,
-                    float* __restrict__ dK, float* __restrict__ dV, int n, int d, float scale,
-                    int causal) {
+                    float* __restrict__ dK, float* __restrict__ dV, HeadMap hm, int n, int d,
+                    float scale, int causal) {
   const int lane = threadIdx.x & 31;
   const int col = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-  const size_t bh = blockIdx.y;
+  const size_t bkv = blockIdx.y;
   if (col >= n) return;
-  const float* kj = K + (bh * n + col) * d;
-  const float* vj = V + (bh * n + col) * d;
-  const float* q = Q + bh * n * d;
-  const float* g = dO + bh * n * d;
+  const float* kj = K + (bkv * n + col) * d;
+  const float* vj = V + (bkv * n + col) * d;
   float kr[kMaxPerLane], vr[kMaxPerLane], ak[kMaxPerLane], av[kMaxPerLane];
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
@@ -171,33 +172,38 @@ bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
     ak[t] = 0.f;
     av[t] = 0.f;
   }
-  for (int i = causal ? col : 0; i < n; ++i) {
-    const float* qi = q + (size_t)i * d;
-    const float* gi = g + (size_t)i * d;
-    float ps = 0.f, pd = 0.f;
+  for (int m = 0; m < hm.group; ++m) {
+    const size_t bh = hm.q_of((int)bkv, m);
+    const float* q = Q + bh * n * d;
+    const float* g = dO + bh * n * d;
+    for (int i = causal ? col : 0; i < n; ++i) {
+      const float* qi = q + (size_t)i * d;
+      const float* gi = g + (size_t)i * d;
+      float ps = 0.f, pd = 0.f;
 #pragma unroll
-    for (int t = 0; t < kMaxPerLane; ++t) {
-      const int c = lane + 32 * t;
-      if (c < d) {
-        ps = fmaf(qi[c], kr[t], ps);
-        pd = fmaf(gi[c], vr[t], pd);
+      for (int t = 0; t < kMaxPerLane; ++t) {
+        const int c = lane + 32 * t;
+        if (c < d) {
+          ps = fmaf(qi[c], kr[t], ps);
+          pd = fmaf(gi[c], vr[t], pd);
+        }
       }
-    }
-    const float s = scale * warp_sum(ps);
-    const float dp = warp_sum(pd);
-    const float p = expf(s - LSE[bh * n + i]);
-    const float ds = p * (dp - Dv[bh * n + i]);
+      const float s = scale * warp_sum(ps);
+      const float dp = warp_sum(pd);
+      const float p = expf(s - LSE[bh * n + i]);
+      const float ds = p * (dp - Dv[bh * n + i]);
 #pragma unroll
-    for (int t = 0; t < kMaxPerLane; ++t) {
-      const int c = lane + 32 * t;
-      if (c < d) {
-        av[t] = fmaf(p, gi[c], av[t]);
-        ak[t] = fmaf(ds, qi[c], ak[t]);
+      for (int t = 0; t < kMaxPerLane; ++t) {
+        const int c = lane + 32 * t;
+        if (c < d) {
+          av[t] = fmaf(p, gi[c], av[t]);
+          ak[t] = fmaf(ds, qi[c], ak[t]);
+        }
       }
     }
   }
-  float* ok = dK + (bh * n + col) * d;
-  float* ov = dV + (bh * n + col) * d;
+  float* ok = dK + (bkv * n + col) * d;
+  float* ov = dV + (bkv * n + col) * d;
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
     const int c = lane + 32 * t;
@@ -211,9 +217,10 @@ bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
 }  // namespace
 
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
-                           int BH, int n, int d, float scale, int causal, cudaStream_t st) {
+                           int BH, const HeadMap& hm, int n, int d, float scale, int causal,
+                           cudaStream_t st) {
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
-  fwd_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, O, LSE, n, d, scale, causal);
+  fwd_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, O, LSE, hm, n, d, scale, causal);
   return cudaGetLastError();
 }
 
@@ -227,18 +234,20 @@ cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH,
 
 cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, const float* dO,
                                 const float* LSE, const float* Dv, float* dK, float* dV, int BH,
-                                int n, int d, float scale, int causal, cudaStream_t st) {
-  dim3 grid(ceil_div(n, kRowsPerBlock), BH);
-  bwd_dkdv_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dK, dV, n, d,
+                                const HeadMap& hm, int n, int d, float scale, int causal,
+                                cudaStream_t st) {
+  dim3 grid(ceil_div(n, kRowsPerBlock), BH / hm.group);
+  bwd_dkdv_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dK, dV, hm, n, d,
                                                            scale, causal);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, const float* dO,
-                              const float* LSE, const float* Dv, float* dQ, int BH, int n, int d,
-                              float scale, int causal, cudaStream_t st) {
+                              const float* LSE, const float* Dv, float* dQ, int BH,
+                              const HeadMap& hm, int n, int d, float scale, int causal,
+                              cudaStream_t st) {
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
-  bwd_dq_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dQ, n, d, scale,
+  bwd_dq_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dQ, hm, n, d, scale,
                                                          causal);
   return cudaGetLastError();
 }

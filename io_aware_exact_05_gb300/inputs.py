@@ -13,6 +13,12 @@ Workloads (batch B, heads H, sequence n, head dim d):
   b1h8_n32k_d128  B1  H8  n32768 d128  bf16  causal      Q,K ~ N(0,4); V,dO ~ N(0,1)
   b2h8_n4k_d256   B2  H8  n4096  d256  bf16  non-causal  N(0,1)
 
+Grouped-query workloads (H query heads sharing H_kv key/value heads; K and
+V are drawn with H_kv heads):
+
+  b2h16kv4_n8k_d128  B2 H16 H_kv 4  n8192 d128 bf16 causal  N(0,1)
+  b1h32kv1_n4k_d128  B1 H32 H_kv 1  n4096 d128 bf16 causal  N(0,1)
+
 Values are drawn in float32 and rounded to bf16 round-to-nearest-even; the
 Q/K factor 2.0 of the sharp-softmax workload is a power of two, so it is
 exact in either dtype.
@@ -22,7 +28,7 @@ from dataclasses import dataclass, replace
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs"]
+__all__ = ["Workload", "WORKLOADS", "GQA_WORKLOADS", "workload", "make_inputs"]
 
 
 @dataclass(frozen=True)
@@ -36,6 +42,11 @@ class Workload:
     causal: bool
     qk_gain: float = 1.0
     seed: int = 0
+    H_kv: int = 0       # key/value heads; 0 means one per query head (H)
+
+    @property
+    def kv_heads(self):
+        return self.H_kv or self.H
 
     @property
     def torch_dtype(self):
@@ -59,25 +70,32 @@ WORKLOADS = [
 ]
 
 
+GQA_WORKLOADS = [
+    Workload("b2h16kv4_n8k_d128", 2, 16, 8192, 128, "bf16", True, 1.0, 1006, H_kv=4),
+    Workload("b1h32kv1_n4k_d128", 1, 32, 4096, 128, "bf16", True, 1.0, 1007, H_kv=1),
+]
+
+
 def workload(name):
-    for w in WORKLOADS:
+    for w in WORKLOADS + GQA_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
 
 
 def make_inputs(w, device="cpu", pin=False):
-    """Draw q, k, v, do of shape (B, H, n, d) for workload ``w``.
+    """Draw q, do of shape (B, H, n, d) and k, v of shape (B, H_kv, n, d)
+    for workload ``w``.
 
     Draw order is fixed (q, k, v, do) from ``torch.Generator().manual_seed(w.seed)``.
     Returns a dict of tensors in ``w.torch_dtype`` on ``device`` (pinned host
     memory if ``pin`` and device is cpu).
     """
     g = torch.Generator(device="cpu").manual_seed(int(w.seed))
-    shape = (w.B, w.H, w.n, w.d)
     out = {}
     for name in ("q", "k", "v", "do"):
-        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        heads = w.kv_heads if name in ("k", "v") else w.H
+        x = torch.randn((w.B, heads, w.n, w.d), generator=g, dtype=torch.float32)
         if name in ("q", "k") and w.qk_gain != 1.0:
             x.mul_(w.qk_gain)
         x = x.to(w.torch_dtype)

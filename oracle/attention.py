@@ -47,7 +47,10 @@ loops with the explicit softmax Jacobian at n <= 8, central finite
 differences of L = sum(dO o O), torch's float64 CPU scaled-dot-product
 attention with autograd, closed forms (Q = 0, n = 1, causal row 0) and
 invariants (rows of P sum to 1, LSE bounds, shift invariances,
-rowsum(dS) = 0, sum_j dV_j = sum_i dO_i, <Q,dQ> = <K,dK>).
+rowsum(dS) = 0, sum_j dV_j = sum_i dO_i, <Q,dQ> = <K,dK>).  The grouped-query
+form (fewer key/value heads) is pinned by central finite differences with
+respect to the shared K and V, and by its one-key/value-head-per-query-head
+special case.
 """
 
 import numpy as np
@@ -172,31 +175,48 @@ def attention_backward_head_sampled(q, k, v, do, scale=None, causal=False,
     return dq, dk, dv, D
 
 
+def _group(H, H_kv):
+    """Query heads per key/value head.  Grouped-query attention ("Flash
+    Attention: Revolutionizing Transformer Efficiency", section
+    FlashAttention-2, item 3): query head h reads key/value head h // g."""
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv = %d must divide H = %d" % (H_kv, H))
+    return H // H_kv
+
+
 def attention_forward(q, k, v, scale=None, causal=False):
-    """Forward over a batch: q, k, v of shape (B, H, n, d).  Returns
-    (O, LSE) as float64 arrays of shape (B, H, n, d) and (B, H, n)."""
+    """Forward over a batch: q of shape (B, H, n, d); k, v of shape
+    (B, H_kv, n, d) with H_kv dividing H (H_kv = H: one key/value head per
+    query head).  Returns (O, LSE) as float64 arrays of shape (B, H, n, d)
+    and (B, H, n)."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, H, n, d = q.shape
+    g = _group(H, k.shape[1])
     o = np.empty((B, H, n, v.shape[-1]))
     lse = np.empty((B, H, n))
     for b in range(B):
         for h in range(H):
             o[b, h], lse[b, h] = attention_forward_head(
-                q[b, h], k[b, h], v[b, h], scale, causal)
+                q[b, h], k[b, h // g], v[b, h // g], scale, causal)
     return o, lse
 
 
 def attention_backward(q, k, v, do, scale=None, causal=False):
-    """Backward over a batch of shape (B, H, n, d).  Returns float64
-    (dQ, dK, dV, D) with D of shape (B, H, n)."""
+    """Backward over a batch (shapes as attention_forward).  Returns float64
+    (dQ, dK, dV, D) with D of shape (B, H, n).  A key/value head read by
+    several query heads gets the sum of the gradients through each of them
+    (the loss depends on it through every head of its group)."""
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     B, H, n, d = q.shape
+    g = _group(H, k.shape[1])
     dq = np.empty_like(q)
-    dk = np.empty_like(k)
-    dv = np.empty_like(v)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
     D = np.empty((B, H, n))
     for b in range(B):
         for h in range(H):
-            dq[b, h], dk[b, h], dv[b, h], D[b, h] = attention_backward_head(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+            dq[b, h], dk_h, dv_h, D[b, h] = attention_backward_head(
+                q[b, h], k[b, h // g], v[b, h // g], do[b, h], scale, causal)
+            dk[b, h // g] += dk_h
+            dv[b, h // g] += dv_h
     return dq, dk, dv, D

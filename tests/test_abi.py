@@ -29,7 +29,8 @@ def _declared():
 
 def test_header_declares_entry_points():
     names = _declared()
-    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status",
+    for n in ("attn_fwd", "attn_bwd", "attn_fwd_gqa", "attn_bwd_gqa", "attn_bwd_workspace_size",
+              "attn_status",
               "attn_strerror", "attn_mat_fwd", "attn_mat_bwd", "attn_gemm_bf16"):
         assert n in names
 
@@ -115,6 +116,27 @@ def test_bwd_argument_checks(L):
     assert call(scale=float("nan")) == 1
     bad = [FAKE] * 8 + [ctypes.c_void_p(0)]
     assert L.attn_bwd(*bad, 1, 2, 256, 128, 0, 0.1, 1, 0, ws, 1 << 30, None) == 1
+
+
+def test_gqa_argument_checks(L):
+    def fwd(H=4, Hkv=2, d=64):
+        return L.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, H, Hkv, 128, d, 0, 0.125, 0, None)
+
+    assert fwd(Hkv=3) == 1       # does not divide H
+    assert fwd(Hkv=0) == 1
+    assert fwd(Hkv=8) == 1       # more key/value heads than query heads
+    assert fwd(d=96) == 2
+    ws = ctypes.c_void_p(1 << 24)
+    assert L.attn_bwd_gqa(*([FAKE] * 9), 1, 4, 3, 256, 128, 0, 0.1, 1, 0, ws, 1 << 30, None) == 1
+    assert L.attn_bwd_gqa(*([FAKE] * 9), 1, 4, 2, 256, 96, 0, 0.1, 1, 0, ws, 1 << 30, None) == 2
+    assert L.attn_bwd_gqa_workspace_size(1, 4, 3, 256, 128, 0, 1, 0) == 0
+    mha = L.attn_bwd_workspace_size(2, 16, 8192, 128, 0, 1, 0)
+    assert L.attn_bwd_gqa_workspace_size(2, 16, 16, 8192, 128, 0, 1, 0) == mha
+    assert L.attn_bwd_gqa_workspace_size(2, 16, 4, 8192, 128, 0, 1, 0) == mha   # no split needed
+    # one key/value head for 32 query heads at n = 4096: the group is split, and the
+    # fp32 dK and dV accumulators (2 x 4096 x 128 x 4 bytes) are added
+    mqa = L.attn_bwd_gqa_workspace_size(1, 32, 1, 4096, 128, 0, 1, 0)
+    assert mqa == L.attn_bwd_workspace_size(1, 32, 4096, 128, 0, 1, 0) + 2 * 4096 * 128 * 4
 
 
 def test_gemm_argument_checks(L):

@@ -357,3 +357,65 @@ def test_quadratic_cost_fixture():
         b = attention_flops(1, 1, n * r["length_ratio"], 64, causal=False)
         assert b["fwd"] == r["cost_ratio"] * a["fwd"]
         assert b["bwd"] == r["cost_ratio"] * a["bwd"]
+
+
+# ---------------------------------------------------------------------------
+# grouped-query attention: H query heads share H_kv key/value heads
+
+
+@pytest.mark.parametrize("H,Hkv,causal", [(4, 2, False), (3, 1, True), (6, 3, True)])
+def test_gqa_finite_differences(H, Hkv, causal):
+    # L = sum over every query head of sum(dO o O); the gradient with respect
+    # to a shared key/value element is checked by central differences, which
+    # knows nothing of how the oracle combines the heads of a group.
+    rng = _rng(50 + H + Hkv)
+    B, n, d = 2, 5, 3
+    q, do = _rand(rng, B, H, n, d), _rand(rng, B, H, n, d)
+    k, v = _rand(rng, B, Hkv, n, d), _rand(rng, B, Hkv, n, d)
+    scale = 0.7
+
+    def loss(kk, vv, qq=q):
+        o, _ = attention_forward(qq, kk, vv, scale, causal)
+        return float((o * do).sum())
+
+    dq, dk, dv, _ = attention_backward(q, k, v, do, scale, causal)
+    assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+    h = 1e-5
+    for which, grad in ((0, dk), (1, dv)):
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            kp, vp = k.copy(), v.copy()
+            km, vm = k.copy(), v.copy()
+            (kp if which == 0 else vp)[idx] += h
+            (km if which == 0 else vm)[idx] -= h
+            fd[idx] = (loss(kp, vp) - loss(km, vm)) / (2 * h)
+        err = np.abs(fd - grad).max() / np.abs(grad).max()
+        assert err < 1e-7, (which, err)
+    fdq = np.zeros_like(dq)
+    for idx in np.ndindex(*dq.shape):
+        qp, qm = q.copy(), q.copy()
+        qp[idx] += h
+        qm[idx] -= h
+        fdq[idx] = (loss(k, v, qp) - loss(k, v, qm)) / (2 * h)
+    assert np.abs(fdq - dq).max() / np.abs(dq).max() < 1e-7
+
+
+def test_gqa_one_kv_head_per_query_head_and_repeat():
+    # H_kv = H is plain multi-head attention; a group of g heads equals
+    # multi-head attention on K, V repeated g times, with dK, dV summed back.
+    rng = _rng(60)
+    B, H, n, d, g = 1, 4, 7, 5, 2
+    q, do = _rand(rng, B, H, n, d), _rand(rng, B, H, n, d)
+    k, v = _rand(rng, B, H // g, n, d), _rand(rng, B, H // g, n, d)
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    o_g, l_g = attention_forward(q, k, v, 0.5, True)
+    o_r, l_r = attention_forward(q, kr, vr, 0.5, True)
+    np.testing.assert_array_equal(o_g, o_r)
+    np.testing.assert_array_equal(l_g, l_r)
+    dq_g, dk_g, dv_g, _ = attention_backward(q, k, v, do, 0.5, True)
+    dq_r, dk_r, dv_r, _ = attention_backward(q, kr, vr, do, 0.5, True)
+    np.testing.assert_array_equal(dq_g, dq_r)
+    np.testing.assert_allclose(dk_g, dk_r.reshape(B, H // g, g, n, d).sum(2), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dv_g, dv_r.reshape(B, H // g, g, n, d).sum(2), rtol=1e-13, atol=1e-14)
+    with pytest.raises(ValueError):
+        attention_forward(q, k[:, :1].repeat(3, axis=1), v[:, :1].repeat(3, axis=1))
