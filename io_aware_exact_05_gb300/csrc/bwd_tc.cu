@@ -85,7 +85,9 @@ struct KvCfg {
 enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8, K_DVD = 9,
              K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13 };
 
-template <int D, bool DQ>
+// GROUPED: query heads share key/value heads (compiled separately so that the
+// one-head-per-head kernel keeps its simple loops).
+template <int D, bool DQ, bool GROUPED>
 __global__ void __launch_bounds__(KvCfg<D, DQ>::NTHREADS, 1)
 bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -116,9 +118,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   // The query heads of this key/value head's group are split over gsplit
   // CTAs; iteration u visits query tile i_start + u % cnt of query head
   // qbase + u / cnt, so dK and dV accumulate over this CTA's part of the
-  // group.  Each loop tracks (tile, head) incrementally.
-  const int gper = hm.group / gsplit;
-  const int qbase = hm.q_of(bh, part * gper);
+  // group.  Each role runs an outer loop over its heads and an inner loop
+  // over the query tiles.
+  const int gper = GROUPED ? hm.group / gsplit : 1;
+  const int qbase = GROUPED ? hm.q_of(bh, part * gper) : bh;
   const int total = gper * cnt;
 
   if (threadIdx.x == 0) {
@@ -159,23 +162,28 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
       }
       int issued_last[2] = {-1, -1};
-      for (int u = 0, ut = 0, bq = qbase; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1,
-               bq += (ut == 0)) {
-        const int s = u % C::STG;
-        const int q0 = (i_start + ut) * C::BM;
-        if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
-          break;
-        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
-        mbar_expect_tx(bar(K_QF + s), 2 * C::QT_BYTES + 2 * C::STAT_BYTES);
+      bool go = true;
+      for (int gi = 0, u = 0; go && gi < gper; ++gi) {
+        const int bq = qbase + gi;
+        for (int ut = 0; ut < cnt; ++ut, ++u) {
+          const int s = u % C::STG;
+          const int q0 = (i_start + ut) * C::BM;
+          if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+            go = false;
+            break;
+          }
+          const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
+          mbar_expect_tx(bar(K_QF + s), 2 * C::QT_BYTES + 2 * C::STAT_BYTES);
 #pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(K_QF + s));
-          tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(K_QF + s));
+          for (int kb = 0; kb < C::NKB; ++kb) {
+            tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(K_QF + s));
+            tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(K_QF + s));
+          }
+          bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bq * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
+          bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bq * n_pad + q0, C::STAT_BYTES,
+                    bar(K_QF + s));
+          issued_last[s] = u;
         }
-        bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bq * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
-        bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bq * n_pad + q0, C::STAT_BYTES,
-                  bar(K_QF + s));
-        issued_last[s] = u;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
@@ -269,82 +277,84 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
-    for (int u = 0, ut = 0; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1) {
-      const int s = u % C::STG;
-      const int q0 = (i_start + ut) * C::BM;
-      const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
-      const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
-      const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
-      ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
-      ok = ok && mbar_wait(bar(K_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      const bool masked = causal && (k0 + C::BNK - 1 > q0);
-      const int qbase = q0 + h * NC;     // first query column of this thread
-      float p[NC];
+    for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
+      for (int ut = 0; ut < cnt; ++ut, ++u) {
+        const int s = u % C::STG;
+        const int q0 = (i_start + ut) * C::BM;
+        const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
+        const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
+        const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
+        ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+        ok = ok && mbar_wait(bar(K_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const bool masked = causal && (k0 + C::BNK - 1 > q0);
+        const int qbase = q0 + h * NC;     // first query column of this thread
+        float p[NC];
 #pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(s_addr + c0, rr);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(s_addr + c0, rr);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
-          if (masked && key > qbase + c0 + i) v = 0.f;
-          p[c0 + i] = v;
+          for (int i = 0; i < 32; ++i) {
+            float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
+            if (masked && key > qbase + c0 + i) v = 0.f;
+            p[c0 + i] = v;
+          }
         }
-      }
 #pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
-        tmem_st16(s_addr + c0 / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(K_PR));
-      ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t ds[NC / 2];
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(dp_addr + c0, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]);
-          const float b = p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]);
-          ds[c0 / 2 + i] = pack_bf16x2(a, b);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
+          tmem_st16(s_addr + c0 / 2, pk);
         }
-      }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(K_PR));
+        ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t ds[NC / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < NC / 2; c0 += 16) {
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < NC; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(dp_addr + c0, rr);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = ds[c0 + i];
-        tmem_st16(dp_addr + c0, pk);
-      }
-      tmem_st_wait();
-      if (C::WITH_DQ) {
-        if (C::DS_ALIAS) {
-          ok = mbar_wait(bar(K_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          for (int i = 0; i < 16; ++i) {
+            const float a = p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]);
+            const float b = p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]);
+            ds[c0 / 2 + i] = pack_bf16x2(a, b);
+          }
         }
-        // dS as the MN-major A operand of dQ = dS K: query block h (64 queries)
-        // is one 128-byte row per key, eight 16-byte chunks, 128-byte swizzle.
-        uint8_t* dsb = C::DS_ALIAS ? const_cast<uint8_t*>(stp) + C::QT_BYTES : smem + C::DS_OFF;
-        uint8_t* rowp = dsb + h * (C::BNK * 128);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
-              make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
-        fence_proxy_async_smem();
+        for (int c0 = 0; c0 < NC / 2; c0 += 16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = ds[c0 + i];
+          tmem_st16(dp_addr + c0, pk);
+        }
+        tmem_st_wait();
+        if (C::WITH_DQ) {
+          if (C::DS_ALIAS) {
+            ok = mbar_wait(bar(K_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          }
+          // dS as the MN-major A operand of dQ = dS K: query block h (64 queries)
+          // is one 128-byte row per key, eight 16-byte chunks, 128-byte swizzle.
+          uint8_t* dsb = C::DS_ALIAS ? const_cast<uint8_t*>(stp) + C::QT_BYTES : smem + C::DS_OFF;
+          uint8_t* rowp = dsb + h * (C::BNK * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
+                make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(K_DSR));
       }
-      tc_fence_before();
-      mbar_arrive(bar(K_DSR));
     }
     // ---- epilogue: half 0 writes dV, half 1 writes dK (scaled)
     if (ok) {
@@ -356,7 +366,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t src = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
       const size_t off = ((size_t)bh * n + key) * D + oh * C::DO;
       const float mul = h == 0 ? 1.f : scale;
-      float* acc = (h == 0 ? dVacc : dKacc);   // set when the group is split over CTAs
+      float* acc = GROUPED ? (h == 0 ? dVacc : dKacc) : nullptr;   // set when the group is split
 #pragma unroll 1
       for (int c0 = 0; c0 < C::DO; c0 += 32) {
         uint32_t rr[32];
@@ -380,33 +390,39 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int q = warp & 3;
     const int r = q * 32 + lane;     // query row within the tile
     const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::S_COL;
-    for (int u = 0, ut = 0, bq = qbase; u < total; ++u, ut = (ut + 1 == cnt) ? 0 : ut + 1,
-             bq += (ut == 0)) {
-      bool ok = mbar_wait(bar(K_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const int qrow = (i_start + ut) * C::BM + r;
-      float* dst = dQacc + ((size_t)bq * n + qrow) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 64) {
-        uint32_t a[32], b[32];
-        tmem_ld32(src + c0, a);
-        tmem_ld32(src + c0 + 32, b);
-        tmem_ld_wait();
-        if (c0 + 64 >= D) {   // all of dQ_i is in registers: release the columns
-          tc_fence_before();
-          mbar_arrive(bar(K_DQE));
+    bool go = true;
+    for (int gi = 0, u = 0; go && gi < gper; ++gi) {
+      const int bq = qbase + gi;
+      for (int ut = 0; ut < cnt; ++ut, ++u) {
+        bool ok = mbar_wait(bar(K_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
+        if (!__all_sync(0xffffffffu, ok)) {
+          go = false;
+          break;
         }
-        if (qrow < n) {
+        tc_fence_after();
+        const int qrow = (i_start + ut) * C::BM + r;
+        float* dst = dQacc + ((size_t)bq * n + qrow) * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t a[32], b[32];
+          tmem_ld32(src + c0, a);
+          tmem_ld32(src + c0 + 32, b);
+          tmem_ld_wait();
+          if (c0 + 64 >= D) {   // all of dQ_i is in registers: release the columns
+            tc_fence_before();
+            mbar_arrive(bar(K_DQE));
+          }
+          if (qrow < n) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dst + c0 + i, scale * __uint_as_float(a[i]), scale * __uint_as_float(a[i + 1]),
-                       scale * __uint_as_float(a[i + 2]), scale * __uint_as_float(a[i + 3]));
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(dst + c0 + i, scale * __uint_as_float(a[i]), scale * __uint_as_float(a[i + 1]),
+                         scale * __uint_as_float(a[i + 2]), scale * __uint_as_float(a[i + 3]));
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dst + c0 + 32 + i, scale * __uint_as_float(b[i]),
-                       scale * __uint_as_float(b[i + 1]), scale * __uint_as_float(b[i + 2]),
-                       scale * __uint_as_float(b[i + 3]));
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(dst + c0 + 32 + i, scale * __uint_as_float(b[i]),
+                         scale * __uint_as_float(b[i + 1]), scale * __uint_as_float(b[i + 2]),
+                         scale * __uint_as_float(b[i + 3]));
+          }
         }
       }
     }
@@ -651,7 +667,7 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
       !make_tmap_bf16(&tv, V, D, n, BHkv, 64, C::BNK) ||
       !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
-  auto kern = bwd_kv_kernel<D, DQ>;
+  auto kern = hm.group > 1 ? bwd_kv_kernel<D, DQ, true> : bwd_kv_kernel<D, DQ, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, C::BNK), BHkv, (D / C::DO) * gsplit);
