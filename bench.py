@@ -32,8 +32,9 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from io_aware_exact_05_gb300.flops import attention_flops  # noqa: E402
-from io_aware_exact_05_gb300.inputs import make_inputs, workload  # noqa: E402
+from io_aware_exact_05_gb300.flops import (attention_flops, kept_entries,  # noqa: E402
+                                           sparse_attention_flops)
+from io_aware_exact_05_gb300.inputs import make_block_mask, make_inputs, workload  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -110,20 +111,38 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ reference arm
+def block_mask_of(w):
+    """The workload's block pattern (uint8 [nb][nb]) or None when dense."""
+    return make_block_mask(w.n, *w.sparse, w.seed) if w.sparse else None
+
+
+def step_flops(w, n=None):
+    """Algorithmic FLOPs of one forward + backward of w (on its first n tokens)."""
+    n = w.n if n is None else n
+    if w.sparse:
+        nb = (n + 127) // 128
+        kept = kept_entries(block_mask_of(w).numpy()[:nb, :nb], n, w.causal)
+        return sparse_attention_flops(w.B, w.H, w.d, kept)
+    return attention_flops(w.B, w.H, n, w.d, w.causal)
+
+
 def oracle_step(w, x, heads, n_sub=None):
     """Float64 CPU oracle forward + backward over the given heads, on the
     first n_sub tokens of each (the whole head by default)."""
     import oracle
 
     m = w.n if n_sub is None else n_sub
+    bm = block_mask_of(w)
+    bm = None if bm is None else bm.numpy().astype(bool)[:(m + 127) // 128, :(m + 127) // 128]
     q, do = (x[n].reshape(w.B * w.H, w.n, w.d) for n in ("q", "do"))
     k, v = (x[n].reshape(w.B * w.kv_heads, w.n, w.d) for n in ("k", "v"))
     g = w.H // w.kv_heads
     for h in heads:
         hk = (h // w.H) * w.kv_heads + (h % w.H) // g   # key/value head of query head h
-        oracle.attention_forward_head(q[h][:m], k[hk][:m], v[hk][:m], w.scale, w.causal)
+        oracle.attention_forward_head(q[h][:m], k[hk][:m], v[hk][:m], w.scale, w.causal,
+                                      None, bm)
         oracle.attention_backward_head(q[h][:m], k[hk][:m], v[hk][:m], do[h][:m], w.scale,
-                                       w.causal)
+                                       w.causal, bm)
 
 
 def cpu_cores():
@@ -143,7 +162,7 @@ def time_oracle(w, x, budget_s=12.0, max_heads=4):
         heads.append(h)
         if t >= budget_s:
             break
-    f = attention_flops(1, len(heads), w.n, w.d, w.causal)["total"]
+    f = step_flops(w)["total"] * len(heads) // (w.B * w.H)
     return {"value": f / t / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": "float64 numpy oracle, forward+backward of %d of %d whole heads of %s "
                       "(%.1f s)" % (len(heads), w.B * w.H, w.name, t)}
@@ -164,7 +183,7 @@ def run_reference(args, w):
     target = min(5.0, 90.0 / max(1, args.steps + args.warmup))
     n_sub = int(round(cal * (target / t_cal) ** 0.5 / 128)) * 128
     n_sub = max(128, min(w.n, n_sub))
-    per_step = attention_flops(1, 1, n_sub, w.d, w.causal)["total"]
+    per_step = step_flops(w, n_sub)["total"] // (w.B * w.H)
     for i in range(args.warmup):
         oracle_step(w, x, [i % (w.B * w.H)], n_sub)
     t0 = time.perf_counter()
@@ -236,9 +255,24 @@ def run_ours(args, w):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
     grouped = w.kv_heads != w.H
+    bmask = block_mask_of(w)
+    if bmask is not None:   # block-sparse: the pattern on the device, list workspaces
+        bmask = bmask.to(dev)
+        fws = torch.empty(attn.attn_fwd_sparse_workspace_size(w.n, w.d), dtype=torch.uint8,
+                          device=dev)
+        work = torch.empty(attn.attn_bwd_sparse_workspace_size(w.B, w.H, w.n, w.d,
+                                                               attn.ATTN_BF16, w.causal, mode),
+                           dtype=torch.uint8, device=dev)
 
     def step(e=None):
         if e: e[0].record(st)
+        if bmask is not None:   # the sparse backward is one call: timed as the dK/dV stage
+            attn.attn_fwd_sparse(q, k, v, o, lse, sc, w.causal, bmask, fws, st)
+            if e: e[1].record(st); e[2].record(st)
+            attn.attn_bwd_sparse(q, k, v, o, do, lse, dq, dk, dv, sc, w.causal, bmask, mode,
+                                 work, st)
+            if e: e[3].record(st); e[4].record(st)
+            return
         if grouped:   # the grouped backward is one call: timed as the dK/dV stage
             attn.attn_fwd_gqa(q, k, v, o, lse, sc, w.causal, st)
             if e: e[1].record(st); e[2].record(st)
@@ -287,7 +321,7 @@ def run_ours(args, w):
     stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(args.steps)) / args.steps
                 for s in range(4)]
 
-    fl = attention_flops(w.B, w.H, w.n, w.d, w.causal)
+    fl = step_flops(w)
     per_step = fl["total"]
     value = per_step * ws_n * args.steps / (el_ms * 1e-3) / 1e12
     pk, src = peaks()
@@ -341,6 +375,9 @@ def run_ours(args, w):
             "pct_of_peak": 100.0 * value / ws_n / peak,
             "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "n": w.n,
                        "d": w.d, "causal": w.causal, "dq_mode": args.mode,
+                       "block_pattern": ({"window": w.sparse[0], "global": w.sparse[1],
+                                          "random": w.sparse[2], "block": 128}
+                                         if w.sparse else None),
                        "parallelism": "replicas x%d (heads independent)" % ws_n,
                        "l2": "inputs larger than L2: Q,K,V,dO = %.0f MB per GPU vs 126 MB L2"
                              % (h2d / 1e6)},

@@ -136,6 +136,42 @@ ATTN_API int attn_bwd(const void* Q, const void* K, const void* V, const void* O
 ATTN_API int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           int B, int H, int H_kv, int n, int d, attn_dtype dtype, float scale,
                           int causal, void* stream);
+/*
+ * Block-sparse exact attention.  A block pattern keeps or drops 128 x 128
+ * blocks of the score matrix: block_mask is a DEVICE uint8 array
+ * [ceil(n/128)][ceil(n/128)] (row = block of 128 queries, column = block of
+ * 128 keys; nonzero = kept), shared by every batch and head.  Scores in
+ * dropped blocks are -inf (and, when causal, j > i as usual); the kept
+ * scores go through the exact softmax, so the result is sparse attention
+ * over the pattern ("Chapter 3.1 -- The cost of attention", section 3:
+ * Longformer's local windows and global tokens, BigBird's random links;
+ * "On the fine-grained I/O complexity of attention backward passes", item
+ * 2: sparse attention with Z_QK kept entries).  A query row whose blocks
+ * keep no score attends to nothing: O = 0, LSE = -inf, zero gradients (the
+ * pages are silent; this is the plain reading).  The kernels visit only the
+ * tiles of kept blocks, from per-tile lists they build in the workspace on
+ * each call (a few microseconds).  One key/value head per query head only
+ * (ATTN_ERR_UNSUPPORTED otherwise); no materialise-P form.
+ *   attn_fwd_sparse : workspace of attn_fwd_sparse_workspace_size(n, d)
+ *                     bytes (256-byte aligned).
+ *   attn_bwd_sparse : workspace of attn_bwd_sparse_workspace_size(...)
+ *                     bytes (the attn_bwd workspace plus the lists).
+ * Other arguments, layouts and errors as attn_fwd / attn_bwd; a null
+ * block_mask is ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API size_t attn_fwd_sparse_workspace_size(int n, int d);
+ATTN_API int attn_fwd_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             int B, int H, int n, int d, attn_dtype dtype, float scale,
+                             int causal, const unsigned char* block_mask, void* workspace,
+                             size_t workspace_bytes, void* stream);
+ATTN_API size_t attn_bwd_sparse_workspace_size(int B, int H, int n, int d, attn_dtype dtype,
+                                               int causal, attn_dq_mode mode);
+ATTN_API int attn_bwd_sparse(const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int H, int n, int d, attn_dtype dtype, float scale,
+                             int causal, attn_dq_mode mode, const unsigned char* block_mask,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 ATTN_API size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int n, int d,
                                             attn_dtype dtype, int causal, attn_dq_mode mode);
 ATTN_API int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,

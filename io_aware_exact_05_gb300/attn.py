@@ -64,6 +64,14 @@ def lib():
             L.attn_bwd_gqa.restype = i
             L.attn_bwd_gqa_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
             L.attn_bwd_gqa_workspace_size.restype = sz
+            L.attn_fwd_sparse_workspace_size.argtypes = [i, i]
+            L.attn_fwd_sparse_workspace_size.restype = sz
+            L.attn_fwd_sparse.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, vp, vp, sz, vp]
+            L.attn_fwd_sparse.restype = i
+            L.attn_bwd_sparse_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.attn_bwd_sparse_workspace_size.restype = sz
+            L.attn_bwd_sparse.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, i, vp, vp, sz, vp]
+            L.attn_bwd_sparse.restype = i
             L.attn_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
             L.attn_bwd_preprocess.restype = i
             L.attn_bwd_dkdv.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -193,6 +201,43 @@ def attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AU
     _check(rc, "attn_bwd_gqa")
 
 
+def attn_fwd_sparse_workspace_size(n, d):
+    return int(lib().attn_fwd_sparse_workspace_size(n, d))
+
+
+def attn_bwd_sparse_workspace_size(B, H, n, d, dtype, causal, mode=ATTN_DQ_AUTO):
+    return int(lib().attn_bwd_sparse_workspace_size(B, H, n, d, dtype, int(bool(causal)),
+                                                    int(mode)))
+
+
+def attn_fwd_sparse(Q, K, V, O, LSE, scale, causal, block_mask, workspace=None, stream=None):
+    """Block-sparse forward; block_mask: uint8 device tensor [ceil(n/128)]^2."""
+    B, H, n, d = _shape(Q)
+    if workspace is None:
+        need = attn_fwd_sparse_workspace_size(n, d)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    rc = lib().attn_fwd_sparse(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, n, d,
+                               _dtype_code(Q), float(scale), int(bool(causal)), _ptr(block_mask),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(rc, "attn_fwd_sparse")
+
+
+def attn_bwd_sparse(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, block_mask,
+                    mode=ATTN_DQ_AUTO, workspace=None, stream=None):
+    """Block-sparse backward (same pattern as the forward)."""
+    B, H, n, d = _shape(Q)
+    dt = _dtype_code(Q)
+    if workspace is None:
+        need = attn_bwd_sparse_workspace_size(B, H, n, d, dt, causal, mode)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=Q.device)
+    rc = lib().attn_bwd_sparse(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                               _ptr(dK), _ptr(dV), B, H, n, d, dt, float(scale),
+                               int(bool(causal)), int(mode), _ptr(block_mask), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_bwd_sparse")
+
+
 def _ws(workspace):
     return _ptr(workspace), workspace.numel() * workspace.element_size()
 
@@ -253,13 +298,16 @@ def attn_gemm_bf16(A, Bm, C, batch, M, N, K, a_kmajor, b_kmajor, alpha=1.0, stre
 
 # ---------------------------------------------------------------- conveniences
 
-def forward(q, k, v, causal=False, scale=None, stream=None):
-    """Allocate O and LSE with torch and run attn_fwd.  Returns (O, LSE)."""
+def forward(q, k, v, causal=False, scale=None, stream=None, block_mask=None):
+    """Allocate O and LSE with torch and run attn_fwd (attn_fwd_gqa when K
+    has fewer heads, attn_fwd_sparse with a block mask).  Returns (O, LSE)."""
     B, H, n, d = _shape(q)
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
-    if k.shape[1] != H:   # grouped-query: fewer key/value heads than query heads
+    if block_mask is not None:
+        attn_fwd_sparse(q, k, v, o, lse, scale, causal, block_mask, None, stream)
+    elif k.shape[1] != H:   # grouped-query: fewer key/value heads than query heads
         attn_fwd_gqa(q, k, v, o, lse, scale, causal, stream)
     else:
         attn_fwd(q, k, v, o, lse, scale, causal, stream)
@@ -267,12 +315,15 @@ def forward(q, k, v, causal=False, scale=None, stream=None):
 
 
 def backward(q, k, v, o, do, lse, causal=False, scale=None, mode=ATTN_DQ_AUTO,
-             workspace=None, stream=None):
+             workspace=None, stream=None, block_mask=None):
     """Allocate dQ, dK, dV with torch and run attn_bwd.  Returns (dQ, dK, dV)."""
     d = q.shape[-1]
     scale = (1.0 / d ** 0.5) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if k.shape[1] != q.shape[1]:
+    if block_mask is not None:
+        attn_bwd_sparse(q, k, v, o, do, lse, dq, dk, dv, scale, causal, block_mask, mode,
+                        workspace, stream)
+    elif k.shape[1] != q.shape[1]:
         attn_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)
     else:
         attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, mode, workspace, stream)

@@ -126,8 +126,29 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; 
 
 extern "C" {
 
-int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                 int H_kv, int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
+// Tile lists of a block pattern for the forward's tiling (carved at `buf`).
+static size_t fwd_lists_bytes(int n, int d) {
+  int qr, qt, kvr;
+  fwd_tiling(d, &qr, &qt, &kvr);
+  return round_up(tile_lists_bytes(n, qr, qt, kvr), kAlign);
+}
+static TileLists build_lists(const uint8_t* mask, int n, int causal, bool outer_is_query, int osz,
+                             int members, int isz, void* buf, cudaStream_t st, int* rc) {
+  TileLists tl;
+  const int nouter = ceil_div(n, osz * members), ninner = ceil_div(n, isz);
+  int* lists = static_cast<int*>(buf);
+  *rc = cuda_rc(launch_tile_lists(mask, n, causal, outer_is_query, osz, members, isz, lists, st));
+  tl.lists = lists;
+  tl.counts = lists + (size_t)nouter * ninner;
+  tl.stride = ninner;
+  return tl;
+}
+
+// Forward for H query heads sharing H_kv key/value heads; with `mask` a
+// block-sparse pattern (bf16 lists carved from `lws`).
+static int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                    int H_kv, int n, int d, attn_dtype dtype, float scale, int causal,
+                    const uint8_t* mask, void* lws, size_t lws_bytes, void* stream) {
   if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return ATTN_ERR_INVALID_ARG;
@@ -135,22 +156,53 @@ int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LS
   if (rc) return rc;
   if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   const HeadMap hm{H, H / H_kv};
+  if (mask && H_kv != H) return ATTN_ERR_UNSUPPORTED;   // block-sparse: one K/V head per head
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
   if (dtype == ATTN_F32) {
     if (d > 256) return ATTN_ERR_UNSUPPORTED;
     return cuda_rc(launch_fwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
                                   static_cast<const float*>(V), static_cast<float*>(O), LSE, BH, hm,
-                                  n, d, scale, causal, st));
+                                  mask, n, d, scale, causal, st));
   }
   if (dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
-  return launch_fwd_tc(Q, K, V, O, LSE, BH, hm, n, d, scale, causal, default_ctl(), st);
+  TileLists tl;
+  if (mask) {
+    if (!lws || (reinterpret_cast<uintptr_t>(lws) % kAlign) || lws_bytes < fwd_lists_bytes(n, d))
+      return ATTN_ERR_WORKSPACE;
+    int qr, qt, kvr;
+    fwd_tiling(d, &qr, &qt, &kvr);
+    tl = build_lists(mask, n, causal, true, qr, qt, kvr, lws, st, &rc);
+    if (rc) return rc;
+  }
+  return launch_fwd_tc(Q, K, V, O, LSE, BH, hm, tl, n, d, scale, causal, default_ctl(), st);
+}
+
+int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int H_kv, int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, H_kv, n, d, dtype, scale, causal, nullptr, nullptr, 0,
+                  stream);
 }
 
 int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
              int n, int d, attn_dtype dtype, float scale, int causal, void* stream) {
-  return attn_fwd_gqa(Q, K, V, O, LSE, B, H, H, n, d, dtype, scale, causal, stream);
+  return fwd_impl(Q, K, V, O, LSE, B, H, H, n, d, dtype, scale, causal, nullptr, nullptr, 0,
+                  stream);
+}
+
+size_t attn_fwd_sparse_workspace_size(int n, int d) {
+  if (n < 1 || d < 1 || d > 256) return 0;
+  return fwd_lists_bytes(n, bf16_head_dim(d) ? d : 128);
+}
+
+int attn_fwd_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                    int H, int n, int d, attn_dtype dtype, float scale, int causal,
+                    const unsigned char* block_mask, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!block_mask) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, B, H, H, n, d, dtype, scale, causal, block_mask, workspace,
+                  workspace_bytes, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int causal,
@@ -229,7 +281,7 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, 
 static int bwd_dkdv_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK,
                          void* dV, int B, int H, int H_kv, int n, int d, attn_dtype dtype,
                          float scale, int causal, attn_dq_mode mode, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+                         size_t workspace_bytes, void* stream, const TileLists& tl = TileLists()) {
   if (!ptrs_ok({Q, K, V, dO, dK, dV})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
@@ -246,7 +298,7 @@ static int bwd_dkdv_impl(const void* Q, const void* K, const void* V, const void
       return ATTN_ERR_CUDA;
   }
   rc = launch_bwd_kv_tc(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr, dK,
-                        dV, w.dk_acc, w.dv_acc, B * H, HeadMap{H, H / H_kv}, w.gsplit, n,
+                        dV, w.dk_acc, w.dv_acc, B * H, HeadMap{H, H / H_kv}, w.gsplit, tl, n,
                         (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
   if (rc || w.gsplit == 1) return rc;
   rc = cuda_rc(launch_dq_convert(w.dk_acc, dK, kv_elems, st));
@@ -256,7 +308,8 @@ static int bwd_dkdv_impl(const void* Q, const void* K, const void* V, const void
 
 static int bwd_dq_impl(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
                        int H, int H_kv, int n, int d, attn_dtype dtype, float scale, int causal,
-                       attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
+                       attn_dq_mode mode, void* workspace, size_t workspace_bytes, void* stream,
+                       const TileLists& tl = TileLists()) {
   if (!ptrs_ok({dQ})) return ATTN_ERR_INVALID_ARG;
   attn_dq_mode m;
   BwdWorkspace w;
@@ -267,7 +320,7 @@ static int bwd_dq_impl(const void* Q, const void* K, const void* V, const void* 
   if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;   // use attn_bwd
   if (m == ATTN_DQ_ATOMIC) return cuda_rc(launch_dq_convert(w.dq_acc, dQ, (size_t)B * H * n * d, st));
   if (!ptrs_ok({Q, K, V, dO})) return ATTN_ERR_INVALID_ARG;
-  return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, HeadMap{H, H / H_kv}, n,
+  return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, HeadMap{H, H / H_kv}, tl, n,
                          (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
 }
 
@@ -285,11 +338,24 @@ int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, voi
                      workspace_bytes, stream);
 }
 
-int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int n,
-                 int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+// Bytes of the key-tile and query-tile lists of a block pattern (bf16).
+static size_t bwd_lists_bytes(int n, int d) {
+  int kr, qr, qr2, kr2;
+  bwd_kv_tiling(d, &kr, &qr);
+  bwd_q_tiling(d, &qr2, &kr2);
+  return round_up(tile_lists_bytes(n, kr, 1, qr), kAlign) +
+         round_up(tile_lists_bytes(n, qr2, 1, kr2), kAlign);
+}
+
+// Backward for H query heads sharing H_kv key/value heads; with `mask` a
+// block-sparse pattern whose lists are carved from the workspace after the
+// dense part.
+static int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int n,
+                    int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                    const uint8_t* mask, void* workspace, size_t workspace_bytes, void* stream) {
   if (!ptrs_ok({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID_ARG;
+  if (mask && H_kv != H) return ATTN_ERR_UNSUPPORTED;
   attn_dq_mode m;
   BwdWorkspace w;
   int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,
@@ -304,27 +370,67 @@ int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, con
     rc = cuda_rc(launch_delta_f32(static_cast<const float*>(O), g, w.delta, BH, n, d, st));
     if (rc) return rc;
     rc = cuda_rc(launch_bwd_dkdv_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dK),
-                                     static_cast<float*>(dV), BH, hm, n, d, scale, causal, st));
+                                     static_cast<float*>(dV), BH, hm, mask, n, d, scale, causal,
+                                     st));
     if (rc) return rc;
-    return cuda_rc(launch_bwd_dq_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dQ), BH, hm, n,
-                                     d, scale, causal, st));
+    return cuda_rc(launch_bwd_dq_f32(q, k, v, g, LSE, w.delta, static_cast<float*>(dQ), BH, hm,
+                                     mask, n, d, scale, causal, st));
+  }
+  TileLists tl_kv, tl_q;
+  if (mask) {
+    if (workspace_bytes < w.bytes + bwd_lists_bytes(n, d)) return ATTN_ERR_WORKSPACE;
+    uint8_t* lbase = static_cast<uint8_t*>(workspace) + w.bytes;
+    int kr, qr;
+    bwd_kv_tiling(d, &kr, &qr);
+    tl_kv = build_lists(mask, n, causal, false, kr, 1, qr, lbase, st, &rc);
+    if (rc) return rc;
+    int qr2, kr2;
+    bwd_q_tiling(d, &qr2, &kr2);
+    tl_q = build_lists(mask, n, causal, true, qr2, 1, kr2,
+                       lbase + round_up(tile_lists_bytes(n, kr, 1, qr), kAlign), st, &rc);
+    if (rc) return rc;
   }
   rc = attn_bwd_preprocess(O, dO, LSE, B, H, n, d, dtype, causal, mode, workspace,
                            workspace_bytes, stream);
   if (rc) return rc;
   rc = bwd_dkdv_impl(Q, K, V, dO, dK, dV, B, H, H_kv, n, d, dtype, scale, causal, mode, workspace,
-                     workspace_bytes, stream);
+                     workspace_bytes, stream, tl_kv);
   if (rc) return rc;
   return bwd_dq_impl(Q, K, V, dO, dQ, B, H, H_kv, n, d, dtype, scale, causal, mode, workspace,
-                     workspace_bytes, stream);
+                     workspace_bytes, stream, tl_q);
+}
+
+int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int H_kv, int n,
+                 int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H_kv, n, d, dtype, scale, causal, mode,
+                  nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t attn_bwd_sparse_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int causal,
+                                      attn_dq_mode mode) {
+  const size_t dense = attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode);
+  if (dense == 0) return 0;
+  return dense + (dtype == ATTN_BF16 ? bwd_lists_bytes(n, d) : 0);
+}
+
+int attn_bwd_sparse(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
+                    attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+                    const unsigned char* block_mask, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!block_mask) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H, n, d, dtype, scale, causal, mode,
+                  block_mask, workspace, workspace_bytes, stream);
 }
 
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int n, int d,
              attn_dtype dtype, float scale, int causal, attn_dq_mode mode, void* workspace,
              size_t workspace_bytes, void* stream) {
-  return attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H, n, d, dtype, scale, causal, mode,
-                      workspace, workspace_bytes, stream);
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H, n, d, dtype, scale, causal, mode,
+                  nullptr, workspace, workspace_bytes, stream);
 }
 
 size_t attn_mat_workspace_size(int B, int H, int n, int d) {

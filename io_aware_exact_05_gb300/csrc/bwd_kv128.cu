@@ -77,16 +77,18 @@ enum : int { B_KV = 0, B_QF = 1, B_QE = 3, B_SF = 5, B_DPF = 6, B_PR = 7, B_DVD 
              B_DQF = 10, B_DQE = 11, B_ACC = 12, B_DRAIN = 13 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
-// one-head-per-head kernel keeps its simple loops).
-template <bool DQ, bool GROUPED>
+// one-head-per-head kernel keeps its simple loops).  SPARSE: a block pattern
+// keeps only some query tiles for this key tile; the CTA walks that list
+// (every listed tile lies in kept blocks) instead of the dense range.
+template <bool DQ, bool GROUPED, bool SPARSE>
 __global__ void __launch_bounds__(DQ ? 512 : 384, 1)
 bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const float* __restrict__ LSE2, const float* __restrict__ Dv,
                   float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
                   __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
-                  float* __restrict__ dVacc, HeadMap hm, int gsplit, int n, int n_pad,
-                  float scale, float scale_log2, int causal, KernelCtl ctl) {
+                  float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n,
+                  int n_pad, float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = Kv128;
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
@@ -102,7 +104,9 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
-  const int cnt = nq - i_start;   // query tiles per query head
+  const int* qlist = SPARSE ? tl.lists + (size_t)kt * tl.stride : nullptr;
+  const int cnt = SPARSE ? tl.counts[kt] : nq - i_start;   // query tiles per query head
+  auto qtile = [&](int ut) { return SPARSE ? (qlist[ut] & 0xFFFF) : i_start + ut; };
   // The query heads of this key/value head's group are split over gsplit
   // CTAs (blockIdx.z); iteration u visits query tile i_start + u % cnt of
   // query head qbase + u / cnt, so dK and dV accumulate over this CTA's part
@@ -153,7 +157,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int bq = qbase + gi;
         for (int ut = 0; ut < cnt; ++ut, ++u) {
           const int s = u % C::STG;
-          const int q0 = (i_start + ut) * C::BM;
+          const int q0 = qtile(ut) * C::BM;
           if (!mbar_wait(bar(B_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
             go = false;
             break;
@@ -231,8 +235,8 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_commit(bar(B_DPF));
       };
       bool ok = mbar_wait_warp(bar(B_KV), 0, abort_flag, ctl, SITE_BWD_KV);
-      if (ok) ok = issue_s(0);
-      if (ok) issue_dp(0);
+      if (ok && total > 0) ok = issue_s(0);
+      if (ok && total > 0) issue_dp(0);
       for (int u = 0; ok && u < total; ++u) {
         const uint32_t so = (u % C::STG) * STG16;
         // dV += P^T dO(u): P^T in the S columns, half h at [64h, 64h+32)
@@ -300,7 +304,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
       for (int ut = 0; ut < cnt; ++ut, ++u) {
         const int s = u % C::STG;
-        const int q0 = (i_start + ut) * C::BM;
+        const int q0 = qtile(ut) * C::BM;
         uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
         const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
         const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
@@ -376,6 +380,10 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
+        if (SPARSE && total == 0) {   // no kept query tile: dK = dV = 0, TMEM never written
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (key < n) {
           if (acc) {
 #pragma unroll
@@ -422,7 +430,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
-        const int row0 = (i_start + ut) * C::BM + 64 * half;
+        const int row0 = qtile(ut) * C::BM + 64 * half;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (lead) bulk_wait_read_all();
@@ -449,11 +457,11 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 2) tmem_dealloc<512>(tmem);
 }
 
-template <bool DQ, bool GROUPED>
+template <bool DQ, bool GROUPED, bool SPARSE>
 int launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
              const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
-             int BH, const HeadMap& hm, int gsplit, int n, int n_pad, float scale, int causal,
-             const KernelCtl& ctl, cudaStream_t st) {
+             int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
+             float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
   using C = Kv128;
   const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg, tdq;
@@ -467,7 +475,7 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
   } else {
     tdq = tq;   // not read
   }
-  auto kern = bwd_kv128_kernel<DQ, GROUPED>;
+  auto kern = bwd_kv128_kernel<DQ, GROUPED, SPARSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -475,7 +483,7 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
   kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
                                               static_cast<__nv_bfloat16*>(dK),
                                               static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
-                                              gsplit, n, n_pad, scale,
+                                              gsplit, tl, n, n_pad, scale,
                                               scale * 1.4426950408889634f, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -484,18 +492,23 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
 
 int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
                         const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
-                        int n_pad, float scale, int causal, const KernelCtl& ctl,
-                        cudaStream_t st) {
-#define ATTN_KV128(DQQ, GRP)                                                                  \
-  return launch<DQQ, GRP>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit, n, \
-                          n_pad, scale, causal, ctl, st)
-  if (hm.group > 1) {
-    if (dQacc) ATTN_KV128(true, true);
-    ATTN_KV128(false, true);
+                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
+                        const TileLists& tl, int n, int n_pad, float scale, int causal,
+                        const KernelCtl& ctl, cudaStream_t st) {
+#define ATTN_KV128(DQQ, GRP, SPR)                                                              \
+  return launch<DQQ, GRP, SPR>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit, \
+                               tl, n, n_pad, scale, causal, ctl, st)
+  if (tl.lists) {   // block-sparse: one key/value head per query head
+    if (hm.group > 1) return ATTN_ERR_UNSUPPORTED;
+    if (dQacc) ATTN_KV128(true, false, true);
+    ATTN_KV128(false, false, true);
   }
-  if (dQacc) ATTN_KV128(true, false);
-  ATTN_KV128(false, false);
+  if (hm.group > 1) {
+    if (dQacc) ATTN_KV128(true, true, false);
+    ATTN_KV128(false, true, false);
+  }
+  if (dQacc) ATTN_KV128(true, false, false);
+  ATTN_KV128(false, false, false);
 #undef ATTN_KV128
 }
 

@@ -104,11 +104,11 @@ extern "C" int attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
     if (launch_delta_f32(static_cast<const float*>(O), g, delta, (int)BH, n, d, st) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (launch_bwd_dkdv_f32(q, k, v, g, LSE, delta, static_cast<float*>(dK),
-                            static_cast<float*>(dV), (int)BH, hm, n, d, scale, causal,
+                            static_cast<float*>(dV), (int)BH, hm, nullptr, n, d, scale, causal,
                             st) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    return launch_bwd_dq_f32(q, k, v, g, LSE, delta, static_cast<float*>(dQ), (int)BH, hm, n, d,
-                             scale, causal, st) == cudaSuccess
+    return launch_bwd_dq_f32(q, k, v, g, LSE, delta, static_cast<float*>(dQ), (int)BH, hm, nullptr,
+                             n, d, scale, causal, st) == cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;
   }
@@ -120,8 +120,8 @@ extern "C" int attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
       cudaSuccess)
     return ATTN_ERR_CUDA;
   int rc = launch_bwd_kv_tc(Q, K, V, dO, lse2, delta, nullptr, dK, dV, nullptr, nullptr, (int)BH,
-                            hm, 1, n, (int)n_pad, d, scale, causal, ctl, st);
+                            hm, 1, TileLists(), n, (int)n_pad, d, scale, causal, ctl, st);
   if (rc) return rc;
-  return launch_bwd_q_tc(Q, K, V, dO, lse2, delta, dQ, (int)BH, hm, n, (int)n_pad, d, scale,
-                         causal, ctl, st);
+  return launch_bwd_q_tc(Q, K, V, dO, lse2, delta, dQ, (int)BH, hm, TileLists(), n, (int)n_pad, d,
+                         scale, causal, ctl, st);
 }

@@ -57,7 +57,9 @@ delta_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restric
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (sub == 0) {
     Dv[prow] = valid ? acc : 0.f;
-    LSE2[prow] = valid ? LSE[row] * 1.4426950408889634f : INFINITY;
+    // +inf (P = 0) on padded rows and on rows that kept no score (LSE = -inf)
+    const float lse = valid ? LSE[row] : -INFINITY;
+    LSE2[prow] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
   }
 }
 

@@ -86,16 +86,17 @@ enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR 
              K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
-// one-head-per-head kernel keeps its simple loops).
-template <int D, bool DQ, bool GROUPED>
+// one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
+// the listed query tiles of a block pattern instead of the dense range.
+template <int D, bool DQ, bool GROUPED, bool SPARSE>
 __global__ void __launch_bounds__(KvCfg<D, DQ>::NTHREADS, 1)
 bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ LSE2, const float* __restrict__ Dv,
               float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
               __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
-              float* __restrict__ dVacc, HeadMap hm, int gsplit, int n, int n_pad, float scale,
-              float scale_log2, int causal, KernelCtl ctl) {
+              float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n, int n_pad,
+              float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = KvCfg<D, DQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -114,7 +115,9 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
-  const int cnt = nq - i_start;   // query tiles per query head (>= 1)
+  const int* qlist = SPARSE ? tl.lists + (size_t)kt * tl.stride : nullptr;
+  const int cnt = SPARSE ? tl.counts[kt] : nq - i_start;   // query tiles per query head
+  auto qtile = [&](int ut) { return SPARSE ? (qlist[ut] & 0xFFFF) : i_start + ut; };
   // The query heads of this key/value head's group are split over gsplit
   // CTAs; iteration u visits query tile i_start + u % cnt of query head
   // qbase + u / cnt, so dK and dV accumulate over this CTA's part of the
@@ -167,7 +170,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int bq = qbase + gi;
         for (int ut = 0; ut < cnt; ++ut, ++u) {
           const int s = u % C::STG;
-          const int q0 = (i_start + ut) * C::BM;
+          const int q0 = qtile(ut) * C::BM;
           if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
             go = false;
             break;
@@ -280,7 +283,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
       for (int ut = 0; ut < cnt; ++ut, ++u) {
         const int s = u % C::STG;
-        const int q0 = (i_start + ut) * C::BM;
+        const int q0 = qtile(ut) * C::BM;
         const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
         const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
         const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
@@ -372,6 +375,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
+        if (SPARSE && total == 0) {   // no kept query tile: dK = dV = 0, TMEM never written
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (key < n) {
           if (acc) {
 #pragma unroll
@@ -400,7 +407,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           break;
         }
         tc_fence_after();
-        const int qrow = (i_start + ut) * C::BM + r;
+        const int qrow = qtile(ut) * C::BM + r;
         float* dst = dQacc + ((size_t)bq * n + qrow) * D;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 64) {
@@ -462,8 +469,8 @@ __global__ void __launch_bounds__(QCfg<D>::NTHREADS, 1)
 bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
              const float* __restrict__ LSE2, const float* __restrict__ Dv,
-             __nv_bfloat16* __restrict__ dQ, HeadMap hm, int n, int n_pad, float scale,
-             float scale_log2, int causal, KernelCtl ctl) {
+             __nv_bfloat16* __restrict__ dQ, HeadMap hm, TileLists tl, int n, int n_pad,
+             float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = QCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -481,7 +488,10 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   const int q0 = it * C::BM;
   const int nkv = (n + C::BN - 1) / C::BN;
   const int jend = causal ? min(nkv - 1, (q0 + C::BM - 1) / C::BN) : nkv - 1;
-  const int cnt = jend + 1;
+  // block-sparse: the key tiles of this query tile's list, in place of 0..jend
+  const int* klist = tl.lists ? tl.lists + (size_t)it * tl.stride : nullptr;
+  const int cnt = klist ? tl.counts[it] : jend + 1;
+  auto ktile = [&](int j) { return klist ? (klist[j] & 0xFFFF) : j; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QF), 1);
@@ -524,8 +534,8 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         mbar_expect_tx(bar(Q_KF + s), 2 * C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, j * C::BN, bkv, bar(Q_KF + s));
-          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, j * C::BN, bkv,
+          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, ktile(j) * C::BN, bkv, bar(Q_KF + s));
+          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, ktile(j) * C::BN, bkv,
                       bar(Q_KF + s));
         }
         issued_last[s] = j;
@@ -595,11 +605,12 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     const float dd = Dv[(size_t)bh * n_pad + qrow];
     bool ok = true;
     for (int j = 0; j < cnt; ++j) {
+      const int k0 = ktile(j) * C::BN;
       ok = mbar_wait(bar(Q_SF), j & 1, abort_flag, ctl, SITE_BWD_S_FULL);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const int kbase = j * C::BN + h * NC;
-      const bool masked = causal && (j * C::BN + C::BN - 1 > q0);
+      const int kbase = k0 + h * NC;
+      const bool masked = causal && (k0 + C::BN - 1 > q0);
       float p[NC];
 #pragma unroll
       for (int c0 = 0; c0 < NC; c0 += 32) {
@@ -644,6 +655,10 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
+        if (cnt == 0) {   // block-sparse tile that keeps nothing: dQ = 0, TMEM never written
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (qrow < n) store32_bf16(dst + c0, rr, scale);
       }
     }
@@ -657,8 +672,8 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 template <int D, bool DQ>
 int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
                   const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
-                  int BH, const HeadMap& hm, int gsplit, int n, int n_pad, float scale, int causal,
-                  const KernelCtl& ctl, cudaStream_t st) {
+                  int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
+                  float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
   using C = KvCfg<D, DQ>;
   const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
@@ -667,22 +682,25 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
       !make_tmap_bf16(&tv, V, D, n, BHkv, 64, C::BNK) ||
       !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
-  auto kern = hm.group > 1 ? bwd_kv_kernel<D, DQ, true> : bwd_kv_kernel<D, DQ, false>;
+  if (tl.lists && hm.group > 1) return ATTN_ERR_UNSUPPORTED;
+  auto kern = tl.lists        ? bwd_kv_kernel<D, DQ, false, true>
+              : hm.group > 1 ? bwd_kv_kernel<D, DQ, true, false>
+                             : bwd_kv_kernel<D, DQ, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, C::BNK), BHkv, (D / C::DO) * gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
-                                           gsplit, n, n_pad, scale, scale * 1.4426950408889634f,
-                                           causal, ctl);
+                                           gsplit, tl, n, n_pad, scale,
+                                           scale * 1.4426950408889634f, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D>
 int launch_q(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-             const float* Dv, void* dQ, int BH, const HeadMap& hm, int n, int n_pad, float scale,
-             int causal, const KernelCtl& ctl, cudaStream_t st) {
+             const float* Dv, void* dQ, int BH, const HeadMap& hm, const TileLists& tl, int n,
+             int n_pad, float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
   using C = QCfg<D>;
   const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
@@ -696,8 +714,8 @@ int launch_q(const void* Q, const void* K, const void* V, const void* dO, const 
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, C::BM), BH);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, static_cast<__nv_bfloat16*>(dQ),
-                                           hm, n, n_pad, scale, scale * 1.4426950408889634f, causal,
-                                           ctl);
+                                           hm, tl, n, n_pad, scale, scale * 1.4426950408889634f,
+                                           causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -705,20 +723,20 @@ int launch_q(const void* Q, const void* K, const void* V, const void* dO, const 
 
 int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
                      const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
-                     int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
-                     cudaStream_t st) {
+                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
+                     const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
+                     const KernelCtl& ctl, cudaStream_t st) {
   if (gsplit < 1 || hm.group % gsplit != 0 || (gsplit > 1 && (!dKacc || !dVacc)))
     return ATTN_ERR_INVALID_ARG;
 #define ATTN_KV(DD, DQQ)                                                                      \
   return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm,    \
-                                gsplit, n, n_pad, scale, causal, ctl, st)
+                                gsplit, tl, n, n_pad, scale, causal, ctl, st)
   const bool dq = dQacc != nullptr;
   switch (d) {
     case 64: if (dq) { ATTN_KV(64, true); } else { ATTN_KV(64, false); }
     case 128:
       return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit,
-                                 n, n_pad, scale, causal, ctl, st);
+                                 tl, n, n_pad, scale, causal, ctl, st);
     case 256: if (dq) return ATTN_ERR_UNSUPPORTED; ATTN_KV(256, false);
     default: return ATTN_ERR_UNSUPPORTED;
   }
@@ -726,15 +744,28 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
 }
 
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
-                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm, int n,
-                    int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
-                    cudaStream_t st) {
+                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm,
+                    const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
+                    const KernelCtl& ctl, cudaStream_t st) {
+#define ATTN_Q(DD) \
+  return launch_q<DD>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, tl, n, n_pad, scale, causal, ctl, st)
   switch (d) {
-    case 64: return launch_q<64>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
-    case 128: return launch_q<128>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
-    case 256: return launch_q<256>(Q, K, V, dO, LSE2, Dv, dQ, BH, hm, n, n_pad, scale, causal, ctl, st);
+    case 64: ATTN_Q(64);
+    case 128: ATTN_Q(128);
+    case 256: ATTN_Q(256);
     default: return ATTN_ERR_UNSUPPORTED;
   }
+#undef ATTN_Q
+}
+
+void bwd_kv_tiling(int d, int* kv_rows, int* query_rows) {
+  *kv_rows = 128;
+  *query_rows = d == 256 ? 64 : 128;
+}
+
+void bwd_q_tiling(int d, int* query_rows, int* kv_rows) {
+  *query_rows = 128;
+  *kv_rows = d == 256 ? 64 : 128;
 }
 
 }  // namespace attn

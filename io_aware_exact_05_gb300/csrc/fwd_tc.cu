@@ -90,13 +90,16 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 }
 
 // GROUPED: query heads share key/value heads (compiled separately so the
-// one-head-per-head kernel does no head arithmetic).
-template <int D, int BN, int QT, bool GROUPED>
+// one-head-per-head kernel does no head arithmetic).  SPARSE: a block
+// pattern keeps only some KV tiles; the CTA walks its list of them (the
+// union over its query tiles, each entry flagging the tiles it is kept for)
+// instead of the dense range.
+template <int D, int BN, int QT, bool GROUPED, bool SPARSE>
 __global__ void __launch_bounds__(FwdCfg<D, BN, QT>::NTHREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-              float* __restrict__ LSE, HeadMap hm, int n, float scale_log2, int causal,
-              KernelCtl ctl) {
+              float* __restrict__ LSE, HeadMap hm, TileLists tl, int n, float scale_log2,
+              int causal, KernelCtl ctl) {
   using C = FwdCfg<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -115,12 +118,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int row0 = cta * (QT * C::BM);
   const int nkv = (n + BN - 1) / BN;
 
+  // SPARSE: list position j holds KV tile tile_at(j) (both query tiles walk
+  // the whole list; a tile masks the entries not kept for it).
+  const int* slist = SPARSE ? tl.lists + (size_t)cta * tl.stride : nullptr;
+  const int slen = SPARSE ? tl.counts[cta] : 0;
+  auto tile_at = [&](int j) { return SPARSE ? (slist[j] & 0xFFFF) : j; };
   TileInfo ti;
   {
     int last[2] = {-1, -1};
     for (int t = 0; t < QT; ++t) {
       const int r0 = row0 + t * C::BM;
-      if (r0 < n) last[t] = causal ? min(nkv - 1, (r0 + C::BM - 1) / BN) : nkv - 1;
+      if (r0 < n)
+        last[t] = SPARSE ? slen - 1 : causal ? min(nkv - 1, (r0 + C::BM - 1) / BN) : nkv - 1;
     }
     ti.last0 = last[0];
     ti.last1 = last[1];
@@ -179,7 +188,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_expect_tx(bar(B_KF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, j * BN, bkv,
+          tma_load_3d(sb + C::K_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmK, kb * 64, tile_at(j) * BN, bkv,
                       bar(B_KF + s));
         last_k[s] = j;
       }
@@ -201,7 +210,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_expect_tx(bar(B_VF + s), C::KV_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_3d(sb + C::V_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmV, kb * 64, j * BN, bkv,
+          tma_load_3d(sb + C::V_OFF + s * C::KV_BYTES + kb * (BN * 128), &tmV, kb * 64, tile_at(j) * BN, bkv,
                       bar(B_VF + s));
         last_v[s] = j;
       }
@@ -294,6 +303,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int j = 0; j <= last; ++j) {
       const int k = unit_pos(t, j, ti);
       const int slot = k & 1;
+      const int ent = SPARSE ? slist[j] : j;   // read before the wait hides its latency
       ok = mbar_wait(bar(B_SF + slot), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_S_FULL);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -307,10 +317,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tmem_ld_wait();
       reg_fence<BN>(sr);
       float* s = reinterpret_cast<float*>(sr);
-      const int col0 = j * BN;
-      const bool need_mask = (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
+      const int col0 = (SPARSE ? (ent & 0xFFFF) : j) * BN;
+      // SPARSE: an entry not kept for this tile (kept only for the other
+      // tile of the CTA) is masked whole
+      const bool dropped = SPARSE && !((ent >> (16 + t)) & 1);
+      const bool need_mask =
+          dropped || (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
       if (need_mask) {
-        const int lim = causal ? min(n, row + 1) : n;   // columns < lim are kept
+        const int lim = dropped ? col0 : causal ? min(n, row + 1) : n;   // columns < lim are kept
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (col0 + c >= lim) s[c] = -INFINITY;
@@ -325,7 +339,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_cand = mx * scale_log2;
       const float m_new = (m_cand > m + 8.0f) ? m_cand : m;
-      const float alpha = ex2(m - m_new);   // 0 on the first tile (m = -inf)
+      // SPARSE: a row can have no kept score yet (m_new = -inf); exponents are
+      // then taken against 0, so P = 0 and alpha = 0 instead of NaN
+      const float m_base = (SPARSE && m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(m - m_base);   // 0 on the first tile (m = -inf)
       float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
 #pragma unroll
@@ -333,8 +350,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[c0 + 2 * i], scale_log2, -m_new));
-          const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale_log2, -m_new));
+          const float p0 = ex2(fmaf(s[c0 + 2 * i], scale_log2, -m_base));
+          const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale_log2, -m_base));
           rs8[(2 * i) & 7] += p0;
           rs8[(2 * i + 1) & 7] += p1;
           pk[i] = pack_bf16x2(p0, p1);
@@ -375,7 +392,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv = 1.f / l;
+        const float inv = (SPARSE && l == 0.f) ? 0.f : 1.f / l;   // no kept score: O = 0
         const uint32_t oa = tmem + lane_off + C::O_COL + t * D;
         const size_t obase = ((size_t)bh * n + row) * D;
 #pragma unroll 1
@@ -390,8 +407,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             store_row_bf16(O + obase + c0, v, inv);
           }
         }
-        if (row < n) LSE[(size_t)bh * n + row] = (m + __log2f(l)) * 0.69314718055994531f;
+        if (row < n)
+          LSE[(size_t)bh * n + row] =
+              (SPARSE && l == 0.f) ? -INFINITY : (m + __log2f(l)) * 0.69314718055994531f;
       }
+    } else if (SPARSE && ok && last < 0 && row < n) {   // nothing kept for this CTA
+      const size_t obase = ((size_t)bh * n + row) * D;
+      for (int c = 0; c < D; c += 8)
+        *reinterpret_cast<uint4*>(O + obase + c) = make_uint4(0u, 0u, 0u, 0u);
+      LSE[(size_t)bh * n + row] = -INFINITY;
     }
   }
 
@@ -402,34 +426,44 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int D, int BN, int QT>
 int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
-               const HeadMap& hm, int n, float scale, int causal, const KernelCtl& ctl,
-               cudaStream_t st) {
+               const HeadMap& hm, const TileLists& tl, int n, float scale, int causal,
+               const KernelCtl& ctl, cudaStream_t st) {
   using C = FwdCfg<D, BN, QT>;
   const int BHkv = BH / hm.group;
+  if (tl.lists && hm.group > 1) return ATTN_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) || !make_tmap_bf16(&tk, K, D, n, BHkv, 64, BN) ||
       !make_tmap_bf16(&tv, V, D, n, BHkv, 64, BN))
     return ATTN_ERR_CUDA;
-  auto kern = hm.group > 1 ? fwd_tc_kernel<D, BN, QT, true> : fwd_tc_kernel<D, BN, QT, false>;
+  auto kern = tl.lists        ? fwd_tc_kernel<D, BN, QT, false, true>
+              : hm.group > 1 ? fwd_tc_kernel<D, BN, QT, true, false>
+                             : fwd_tc_kernel<D, BN, QT, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(n, QT * C::BM), BH);
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, hm, n,
-                                           scale_log2, causal, ctl);
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, hm, tl,
+                                           n, scale_log2, causal, ctl);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
 
+void fwd_tiling(int d, int* query_rows, int* query_tiles, int* kv_rows) {
+  *query_rows = 128;
+  *query_tiles = d == 256 ? 1 : 2;
+  *kv_rows = d == 256 ? 64 : 128;
+}
+
 int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
-                  const HeadMap& hm, int n, int d, float scale, int causal, const KernelCtl& ctl,
-                  cudaStream_t st) {
+                  const HeadMap& hm, const TileLists& tl, int n, int d, float scale, int causal,
+                  const KernelCtl& ctl, cudaStream_t st) {
   switch (d) {
-    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
-    case 128: return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
-    case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, hm, n, scale, causal, ctl, st);
+    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
+    case 128:
+      return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
+    case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
     default: return ATTN_ERR_UNSUPPORTED;
   }
 }

@@ -22,21 +22,32 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
 
 KernelCtl default_ctl();
 
+// Block-sparse tile lists (built by launch_tile_lists in sparse.cu): for
+// outer unit u, lists[u * stride + p], p < counts[u], are the inner tiles to
+// visit in increasing order, each entry the tile index (low 16 bits) with one
+// bit per member tile of the unit (bit 16 + m) for "kept for member m".
+struct TileLists {
+  const int* lists = nullptr;   // null: dense
+  const int* counts = nullptr;
+  int stride = 0;
+};
+
 // ---- fp32 SIMT path --------------------------------------------------------
 // BH counts query heads (B * H); K, V (and dK, dV) hold BH / hm.group heads.
+// bmask: block-sparse pattern, uint8 [ceil(n/128)][ceil(n/128)] (null: dense).
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
-                           int BH, const HeadMap& hm, int n, int d, float scale, int causal,
-                           cudaStream_t st);
+                           int BH, const HeadMap& hm, const uint8_t* bmask, int n, int d,
+                           float scale, int causal, cudaStream_t st);
 cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH, int n, int d,
                              cudaStream_t st);
 cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, const float* dO,
                                 const float* LSE, const float* Dv, float* dK, float* dV, int BH,
-                                const HeadMap& hm, int n, int d, float scale, int causal,
-                                cudaStream_t st);
+                                const HeadMap& hm, const uint8_t* bmask, int n, int d, float scale,
+                                int causal, cudaStream_t st);
 cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, const float* dO,
                               const float* LSE, const float* Dv, float* dQ, int BH,
-                              const HeadMap& hm, int n, int d, float scale, int causal,
-                              cudaStream_t st);
+                              const HeadMap& hm, const uint8_t* bmask, int n, int d, float scale,
+                              int causal, cudaStream_t st);
 
 // ---- bf16 helpers ------------------------------------------------------------
 cudaError_t launch_delta_bf16(const void* O, const void* dO, const float* LSE, float* Dv,
@@ -49,9 +60,13 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, in
                      bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
                      cudaStream_t st);
 
+// tl.lists != null: block-sparse (one key/value head per query head only).
 int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
-                  const HeadMap& hm, int n, int d, float scale, int causal, const KernelCtl& ctl,
-                  cudaStream_t st);
+                  const HeadMap& hm, const TileLists& tl, int n, int d, float scale, int causal,
+                  const KernelCtl& ctl, cudaStream_t st);
+// The forward's tiling for head dim d: a CTA owns query_tiles tiles of
+// query_rows rows and walks KV tiles of kv_rows keys.
+void fwd_tiling(int d, int* query_rows, int* query_tiles, int* kv_rows);
 
 // Key-tile backward: dK, dV (and, with dQacc != nullptr, atomic dQ shares).
 // One CTA per (key tile, key/value head, part of the group) walks the query
@@ -59,23 +74,35 @@ int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* L
 // memory.  gsplit = 1: one part, dK and dV stored as bf16.  gsplit > 1: each
 // part adds its sums into the fp32 accumulators dKacc, dVacc (zeroed by the
 // caller; dK already scaled), which the caller converts.
+// tl.lists != null: block-sparse, each key tile walking its listed query
+// tiles (one key/value head per query head only).
 int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
                      const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
-                     int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
-                     cudaStream_t st);
+                     float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
+                     const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
+                     const KernelCtl& ctl, cudaStream_t st);
+// Tiling of the key-tile kernel for head dim d (key tiles of kv_rows keys,
+// query tiles of query_rows).
+void bwd_kv_tiling(int d, int* kv_rows, int* query_rows);
 // Key-tile backward for d = 128, pipelined two query tiles deep (dQ shares
 // reduced into dQacc with TMA bulk reduce-add when dQacc != nullptr).
 int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
                         const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
-                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit, int n,
-                        int n_pad, float scale, int causal, const KernelCtl& ctl,
-                        cudaStream_t st);
+                        float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
+                        const TileLists& tl, int n, int n_pad, float scale, int causal,
+                        const KernelCtl& ctl, cudaStream_t st);
 // Query-tile backward: dQ with no atomics.
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
-                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm, int n,
-                    int n_pad, int d, float scale, int causal, const KernelCtl& ctl,
-                    cudaStream_t st);
+                    const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm,
+                    const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
+                    const KernelCtl& ctl, cudaStream_t st);
+// Tiling of the query-tile dQ kernel (query tiles of query_rows, key tiles of kv_rows).
+void bwd_q_tiling(int d, int* query_rows, int* kv_rows);
+
+// ---- block-sparse tile lists (sparse.cu) ----------------------------------------------
+size_t tile_lists_bytes(int n, int osz, int members, int isz);
+cudaError_t launch_tile_lists(const uint8_t* mask, int n, int causal, bool outer_is_query, int osz,
+                              int members, int isz, int* buf, cudaStream_t st);
 
 // ---- materialise-P row kernels ----------------------------------------------------
 cudaError_t launch_mat_softmax(const float* S, void* P, float* LSE, int BH, int n, float scale,

@@ -29,7 +29,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
 fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                const float* __restrict__ V, float* __restrict__ O, float* __restrict__ LSE,
-               HeadMap hm, int n, int d, float scale, int causal) {
+               HeadMap hm, const uint8_t* __restrict__ bmask, int n, int d, float scale,
+               int causal) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const size_t bh = blockIdx.y;
@@ -38,6 +39,8 @@ fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
   const float* q = Q + (bh * n + row) * d;
   const float* k = K + bkv * n * d;
   const float* v = V + bkv * n * d;
+  // block-sparse pattern (null: dense): the 128-block row of this query
+  const uint8_t* brow = bmask ? bmask + (size_t)(row / 128) * ((n + 127) / 128) : nullptr;
   float qr[kMaxPerLane], acc[kMaxPerLane];
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
@@ -48,6 +51,7 @@ fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
   float m = -INFINITY, l = 0.f;
   const int jend = causal ? row + 1 : n;
   for (int j = 0; j < jend; ++j) {
+    if (brow && !brow[j / 128]) continue;   // key outside the kept blocks
     const float* kj = k + (size_t)j * d;
     float part = 0.f;
 #pragma unroll
@@ -68,14 +72,14 @@ fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
     }
     m = m_new;
   }
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;   // no kept key: O = 0, LSE = -inf
   float* o = O + (bh * n + row) * d;
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
     const int c = lane + 32 * t;
     if (c < d) o[c] = acc[t] * inv;
   }
-  if (lane == 0) LSE[bh * n + row] = m + logf(l);
+  if (lane == 0) LSE[bh * n + row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 // D_i = dO_i . O_i for fp32 tensors (one warp per row).
@@ -98,7 +102,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 bwd_dq_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                   const float* __restrict__ V, const float* __restrict__ dO,
                   const float* __restrict__ LSE, const float* __restrict__ Dv,
-                  float* __restrict__ dQ, HeadMap hm, int n, int d, float scale, int causal) {
+                  float* __restrict__ dQ, HeadMap hm, const uint8_t* __restrict__ bmask, int n,
+                  int d, float scale, int causal) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const size_t bh = blockIdx.y;
@@ -110,6 +115,7 @@ bwd_dq_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
   const float* v = V + bkv * n * d;
   const float lse = LSE[bh * n + row];
   const float Di = Dv[bh * n + row];
+  const uint8_t* brow = bmask ? bmask + (size_t)(row / 128) * ((n + 127) / 128) : nullptr;
   float qr[kMaxPerLane], gr[kMaxPerLane], acc[kMaxPerLane];
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) {
@@ -120,6 +126,7 @@ bwd_dq_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
   }
   const int jend = causal ? row + 1 : n;
   for (int j = 0; j < jend; ++j) {
+    if (brow && !brow[j / 128]) continue;   // key outside the kept blocks
     const float* kj = k + (size_t)j * d;
     const float* vj = v + (size_t)j * d;
     float ps = 0.f, pd = 0.f;
@@ -155,8 +162,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                     const float* __restrict__ V, const float* __restrict__ dO,
                     const float* __restrict__ LSE, const float* __restrict__ Dv,
-                    float* __restrict__ dK, float* __restrict__ dV, HeadMap hm, int n, int d,
-                    float scale, int causal) {
+                    float* __restrict__ dK, float* __restrict__ dV, HeadMap hm,
+                    const uint8_t* __restrict__ bmask, int n, int d, float scale, int causal) {
   const int lane = threadIdx.x & 31;
   const int col = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const size_t bkv = blockIdx.y;
@@ -177,6 +184,7 @@ bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
     const float* q = Q + bh * n * d;
     const float* g = dO + bh * n * d;
     for (int i = causal ? col : 0; i < n; ++i) {
+      if (bmask && !bmask[(size_t)(i / 128) * ((n + 127) / 128) + col / 128]) continue;
       const float* qi = q + (size_t)i * d;
       const float* gi = g + (size_t)i * d;
       float ps = 0.f, pd = 0.f;
@@ -217,10 +225,11 @@ bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
 }  // namespace
 
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
-                           int BH, const HeadMap& hm, int n, int d, float scale, int causal,
-                           cudaStream_t st) {
+                           int BH, const HeadMap& hm, const uint8_t* bmask, int n, int d,
+                           float scale, int causal, cudaStream_t st) {
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
-  fwd_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, O, LSE, hm, n, d, scale, causal);
+  fwd_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, O, LSE, hm, bmask, n, d, scale,
+                                                      causal);
   return cudaGetLastError();
 }
 
@@ -234,21 +243,21 @@ cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH,
 
 cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, const float* dO,
                                 const float* LSE, const float* Dv, float* dK, float* dV, int BH,
-                                const HeadMap& hm, int n, int d, float scale, int causal,
-                                cudaStream_t st) {
+                                const HeadMap& hm, const uint8_t* bmask, int n, int d, float scale,
+                                int causal, cudaStream_t st) {
   dim3 grid(ceil_div(n, kRowsPerBlock), BH / hm.group);
-  bwd_dkdv_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dK, dV, hm, n, d,
-                                                           scale, causal);
+  bwd_dkdv_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dK, dV, hm, bmask,
+                                                           n, d, scale, causal);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, const float* dO,
                               const float* LSE, const float* Dv, float* dQ, int BH,
-                              const HeadMap& hm, int n, int d, float scale, int causal,
-                              cudaStream_t st) {
+                              const HeadMap& hm, const uint8_t* bmask, int n, int d, float scale,
+                              int causal, cudaStream_t st) {
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
-  bwd_dq_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dQ, hm, n, d, scale,
-                                                         causal);
+  bwd_dq_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dQ, hm, bmask, n, d,
+                                                         scale, causal);
   return cudaGetLastError();
 }
 

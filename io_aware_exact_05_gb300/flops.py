@@ -8,7 +8,8 @@ quadratic cost described in "Chapter 3.1 -- The cost of attention",
 section 2.
 """
 
-__all__ = ["attention_flops", "score_entries", "algorithmic_bytes"]
+__all__ = ["attention_flops", "score_entries", "algorithmic_bytes", "kept_entries",
+           "sparse_attention_flops"]
 
 
 def score_entries(n):
@@ -33,3 +34,29 @@ def algorithmic_bytes(B, H, n, d, elt):
     t = B * H * n * d * elt
     r = B * H * n * 4
     return {"fwd": 4 * t + r, "pre": 2 * t + r, "bwd": 7 * t + 2 * r}
+
+
+def kept_entries(block_mask, n, causal, block=128):
+    """Score entries a block pattern keeps (per head): the entries of every
+    kept block clipped to n x n, without j > i when causal."""
+    import numpy as np
+
+    m = np.asarray(block_mask, dtype=bool)
+    nb = m.shape[0]
+    sizes = np.minimum(block, n - np.arange(nb) * block)       # rows (or keys) per block
+    total = 0
+    for bi in range(nb):
+        for bj in np.nonzero(m[bi])[0]:
+            if not causal or bj < bi:
+                total += int(sizes[bi]) * int(sizes[bj])
+            elif bj == bi:                                     # lower triangle of a diagonal block
+                s = int(sizes[bi])
+                total += s * (s + 1) // 2
+    return total
+
+
+def sparse_attention_flops(B, H, d, kept):
+    """FLOPs per call of block-sparse attention: 4 d (fwd) and 10 d (bwd) per
+    kept score entry and head (the dense counts with n^2 -> kept entries)."""
+    fwd, bwd = 4 * B * H * d * kept, 10 * B * H * d * kept
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}

@@ -19,6 +19,13 @@ V are drawn with H_kv heads):
   b2h16kv4_n8k_d128  B2 H16 H_kv 4  n8192 d128 bf16 causal  N(0,1)
   b1h32kv1_n4k_d128  B1 H32 H_kv 1  n4096 d128 bf16 causal  N(0,1)
 
+Block-sparse workloads (a 128 x 128-block pattern shared by every head, from
+make_block_mask: a local window of w blocks on each side of the diagonal,
+g global blocks that attend to and are attended by every block, and r
+random blocks per block row, as in Longformer and BigBird):
+
+  b2h16_n16k_d128_sparse  B2 H16 n16384 d128 bf16 non-causal  w 2, g 1, r 2
+
 Values are drawn in float32 and rounded to bf16 round-to-nearest-even; the
 Q/K factor 2.0 of the sharp-softmax workload is a power of two, so it is
 exact in either dtype.
@@ -28,7 +35,8 @@ from dataclasses import dataclass, replace
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "GQA_WORKLOADS", "workload", "make_inputs"]
+__all__ = ["Workload", "WORKLOADS", "GQA_WORKLOADS", "SPARSE_WORKLOADS", "workload",
+           "make_inputs", "make_block_mask"]
 
 
 @dataclass(frozen=True)
@@ -43,6 +51,7 @@ class Workload:
     qk_gain: float = 1.0
     seed: int = 0
     H_kv: int = 0       # key/value heads; 0 means one per query head (H)
+    sparse: tuple = ()  # (window, global, random) blocks of a block mask; () = dense
 
     @property
     def kv_heads(self):
@@ -76,8 +85,14 @@ GQA_WORKLOADS = [
 ]
 
 
+SPARSE_WORKLOADS = [
+    Workload("b2h16_n16k_d128_sparse", 2, 16, 16384, 128, "bf16", False, 1.0, 1008,
+             sparse=(2, 1, 2)),
+]
+
+
 def workload(name):
-    for w in WORKLOADS + GQA_WORKLOADS:
+    for w in WORKLOADS + GQA_WORKLOADS + SPARSE_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
@@ -105,3 +120,19 @@ def make_inputs(w, device="cpu", pin=False):
             x = x.pin_memory()
         out[name] = x
     return out
+
+
+def make_block_mask(n, window, n_global, n_random, seed, block=128):
+    """A uint8 (ceil(n/block), ceil(n/block)) block pattern: block (i, j) is 1
+    when |i - j| <= window, when i < n_global or j < n_global, or when j is one
+    of n_random distinct blocks drawn for row i from a seeded generator."""
+    nb = (n + block - 1) // block
+    i = torch.arange(nb)[:, None]
+    j = torch.arange(nb)[None, :]
+    m = ((i - j).abs() <= window) | (i < n_global) | (j < n_global)
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    for row in range(nb):
+        if n_random > 0:
+            pick = torch.randperm(nb, generator=g)[:min(n_random, nb)]
+            m[row, pick] = True
+    return m.to(torch.uint8)

@@ -35,6 +35,18 @@ What is computed (per head, Q, K, V, dO of shape (n, d)):
   causal   -- optional mask s_ij = -inf for j > i, applied before the row
               maximum (so P_ij = 0 there).  Every row keeps j = i.
 
+  block mask -- optional block-sparse pattern: a boolean matrix over blocks
+              of `block` (default 128) query rows x `block` keys; scores in
+              a False block are -inf, the rest are exact.  This is sparse
+              attention over a block pattern ("Chapter 3.1", section 3:
+              local windows, global tokens and random links of Longformer
+              and BigBird; "On the fine-grained I/O complexity of attention
+              backward passes", item 2, sparse attention with Z_QK kept
+              entries), computed exactly on the kept entries.  The pages
+              are silent on a row with no kept score; the plain reading
+              taken here is that it attends to nothing: O_i = 0,
+              LSE_i = -inf, and it contributes nothing to any gradient.
+
 Each step is the definition written out with numpy float64 arithmetic; the
 only library primitive is the matrix product.  Large heads are processed a
 group of query rows at a time purely to bound memory: every row is computed
@@ -85,30 +97,50 @@ def _as_f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def _scores(q_rows, k, scale, row_index, causal):
+def _scores(q_rows, k, scale, row_index, causal, block_mask=None, block=128):
     """s_ij = scale * q_i . k_j for the requested query rows i; -inf where
-    the causal mask removes j > i."""
+    the causal mask removes j > i, and where the block mask removes the
+    (i // block, j // block) block."""
     s = scale * (q_rows @ k.T)
     if causal:
         cols = np.arange(k.shape[0])[None, :]
         s = np.where(cols > row_index[:, None], -np.inf, s)
+    if block_mask is not None:
+        keep = np.asarray(block_mask, dtype=bool)[row_index // block][:, np.arange(k.shape[0]) // block]
+        s = np.where(keep, s, -np.inf)
     return s
 
 
 def _row_softmax(s):
     """Two-pass softmax of each row: subtract the row maximum, exponentiate,
-    divide by the row sum.  Returns P, the row maximum m and the row sum l."""
+    divide by the row sum.  Returns P, the row maximum m and the row sum l.
+    A row with no finite score (every key masked) has P = 0, m = -inf and
+    l = 0."""
     m = s.max(axis=1)
-    e = np.exp(s - m[:, None])
+    empty = ~np.isfinite(m)
+    e = np.exp(s - np.where(empty, 0.0, m)[:, None])   # exp(-inf) = 0 off the mask
     l = e.sum(axis=1)
-    return e / l[:, None], m, l
+    p = e / np.where(empty, 1.0, l)[:, None]
+    return p, m, l
 
 
-def attention_forward_head(q, k, v, scale=None, causal=False, rows=None):
+def _lse(m, l):
+    """LSE = m + ln l, and -inf for a row with no kept score (l = 0)."""
+    out = np.full(m.shape, -np.inf)
+    ok = l > 0
+    out[ok] = m[ok] + np.log(l[ok])
+    return out
+
+
+def attention_forward_head(q, k, v, scale=None, causal=False, rows=None, block_mask=None,
+                           block=128):
     """Forward pass of one head.
 
     q, k, v: (n, d).  rows: optional 1-D array of query indices to compute
-    (default: all).  Returns (O[rows], LSE[rows]) in float64.
+    (default: all).  block_mask: optional boolean (ceil(n/block), ceil(n/block))
+    array; scores outside its True blocks are masked (block-sparse exact
+    attention).  Returns (O[rows], LSE[rows]) in float64; a row with no kept
+    score gets O = 0 and LSE = -inf.
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     n, d = q.shape
@@ -119,25 +151,27 @@ def attention_forward_head(q, k, v, scale=None, causal=False, rows=None):
     lse = np.empty(rows.size, dtype=np.float64)
     for g in range(0, rows.size, _ROW_GROUP):
         r = rows[g:g + _ROW_GROUP]
-        s = _scores(q[r], k, scale, r, causal)
+        s = _scores(q[r], k, scale, r, causal, block_mask, block)
         p, m, l = _row_softmax(s)
         o[g:g + r.size] = p @ v
-        lse[g:g + r.size] = m + np.log(l)
+        lse[g:g + r.size] = _lse(m, l)
     return o, lse
 
 
-def attention_backward_head(q, k, v, do, scale=None, causal=False):
+def attention_backward_head(q, k, v, do, scale=None, causal=False, block_mask=None,
+                            block=128):
     """Backward pass of one head: exact gradients (dQ, dK, dV) of
     L = sum(dO o O) with respect to Q, K and V, plus D (length n)."""
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     n, d = q.shape
     return attention_backward_head_sampled(q, k, v, do, scale, causal,
                                            q_rows=np.arange(n),
-                                           k_rows=np.arange(n))
+                                           k_rows=np.arange(n),
+                                           block_mask=block_mask, block=block)
 
 
 def attention_backward_head_sampled(q, k, v, do, scale=None, causal=False,
-                                    q_rows=None, k_rows=None):
+                                    q_rows=None, k_rows=None, block_mask=None, block=128):
     """Backward pass of one head, returning only the requested rows.
 
     dQ is returned for the query indices ``q_rows``; dK and dV for the key
@@ -161,7 +195,7 @@ def attention_backward_head_sampled(q, k, v, do, scale=None, causal=False,
     D = np.empty(n)
     for g in range(0, n, _ROW_GROUP):
         r = np.arange(g, min(g + _ROW_GROUP, n))
-        s = _scores(q[r], k, scale, r, causal)
+        s = _scores(q[r], k, scale, r, causal, block_mask, block)
         p, _, _ = _row_softmax(s)                 # P rows i in r
         dp = do[r] @ v.T                          # dP_ij = dO_i . v_j
         D[r] = (p * dp).sum(axis=1)               # D_i = sum_j P_ij dP_ij
@@ -184,7 +218,7 @@ def _group(H, H_kv):
     return H // H_kv
 
 
-def attention_forward(q, k, v, scale=None, causal=False):
+def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, block=128):
     """Forward over a batch: q of shape (B, H, n, d); k, v of shape
     (B, H_kv, n, d) with H_kv dividing H (H_kv = H: one key/value head per
     query head).  Returns (O, LSE) as float64 arrays of shape (B, H, n, d)
@@ -197,11 +231,11 @@ def attention_forward(q, k, v, scale=None, causal=False):
     for b in range(B):
         for h in range(H):
             o[b, h], lse[b, h] = attention_forward_head(
-                q[b, h], k[b, h // g], v[b, h // g], scale, causal)
+                q[b, h], k[b, h // g], v[b, h // g], scale, causal, None, block_mask, block)
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale=None, causal=False):
+def attention_backward(q, k, v, do, scale=None, causal=False, block_mask=None, block=128):
     """Backward over a batch (shapes as attention_forward).  Returns float64
     (dQ, dK, dV, D) with D of shape (B, H, n).  A key/value head read by
     several query heads gets the sum of the gradients through each of them
@@ -216,7 +250,7 @@ def attention_backward(q, k, v, do, scale=None, causal=False):
     for b in range(B):
         for h in range(H):
             dq[b, h], dk_h, dv_h, D[b, h] = attention_backward_head(
-                q[b, h], k[b, h // g], v[b, h // g], do[b, h], scale, causal)
+                q[b, h], k[b, h // g], v[b, h // g], do[b, h], scale, causal, block_mask, block)
             dk[b, h // g] += dk_h
             dv[b, h // g] += dv_h
     return dq, dk, dv, D

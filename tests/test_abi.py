@@ -139,6 +139,22 @@ def test_gqa_argument_checks(L):
     assert mqa == L.attn_bwd_workspace_size(1, 32, 4096, 128, 0, 1, 0) + 2 * 4096 * 128 * 4
 
 
+def test_sparse_argument_checks(L):
+    ws = ctypes.c_void_p(1 << 24)
+    # null block mask
+    assert L.attn_fwd_sparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 128, 0, 0.1, 0, None, ws,
+                             1 << 20, None) == 1
+    # list workspace too small
+    assert L.attn_fwd_sparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 128, 0, 0.1, 0, FAKE, ws,
+                             16, None) == 3
+    assert L.attn_fwd_sparse_workspace_size(0, 128) == 0
+    assert L.attn_fwd_sparse_workspace_size(256, 128) > 0
+    dense = L.attn_bwd_workspace_size(1, 2, 4096, 128, 0, 1, 0)
+    assert L.attn_bwd_sparse_workspace_size(1, 2, 4096, 128, 0, 1, 0) > dense
+    assert L.attn_bwd_sparse(*([FAKE] * 9), 1, 2, 256, 128, 0, 0.1, 1, 0, None, ws, 1 << 30,
+                             None) == 1
+
+
 def test_gemm_argument_checks(L):
     g = L.attn_gemm_bf16
     assert g(FAKE, FAKE, FAKE, 1, 128, 128, 60, 1, 1, 1, 1.0, None) == 2   # K % 8
@@ -155,3 +171,19 @@ def test_flop_counts():
     assert f["fwd"] == 4 * 2 * 16 * 8192 ** 2 * 128 // 2
     assert f["bwd"] == 10 * 2 * 16 * 8192 ** 2 * 128 // 2
     assert abs(f["bwd"] / 1e12 - 1.374) < 1e-3
+
+
+def test_kept_entries_counts_the_pattern():
+    # the FLOP count of a block pattern: brute-force count of kept (i, j) pairs
+    import numpy as np
+
+    from io_aware_exact_05_gb300.flops import kept_entries
+
+    rng = np.random.default_rng(3)
+    for n, causal in ((300, False), (300, True), (129, True), (520, False)):
+        nb = (n + 127) // 128
+        m = rng.random((nb, nb)) < 0.5
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        keep = m[i // 128, j // 128] & ((j <= i) if causal else True)
+        assert kept_entries(m, n, causal) == int(keep.sum())

@@ -419,3 +419,90 @@ def test_gqa_one_kv_head_per_query_head_and_repeat():
     np.testing.assert_allclose(dv_g, dv_r.reshape(B, H // g, g, n, d).sum(2), rtol=1e-13, atol=1e-14)
     with pytest.raises(ValueError):
         attention_forward(q, k[:, :1].repeat(3, axis=1), v[:, :1].repeat(3, axis=1))
+
+
+# ---------------------------------------------------------------------------
+# block-sparse attention: scores outside the kept blocks are removed
+
+
+def _sparse_rows_loop(q, k, v, scale, causal, mask, block):
+    # per row: a plain softmax over the kept keys only, written with loops
+    n = q.shape[0]
+    o = np.zeros_like(v)
+    lse = np.full(n, -np.inf)
+    for i in range(n):
+        keys = [j for j in range(n)
+                if mask[i // block, j // block] and (not causal or j <= i)]
+        if not keys:
+            continue
+        s = [scale * sum(q[i, c] * k[j, c] for c in range(q.shape[1])) for j in keys]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        tot = sum(e)
+        lse[i] = m + math.log(tot)
+        for jj, j in enumerate(keys):
+            o[i] += e[jj] / tot * v[j]
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_matches_kept_key_loops(causal):
+    rng = _rng(70 + causal)
+    n, d, block = 22, 3, 4
+    q, k, v = (_rand(rng, n, d) for _ in range(3))
+    nb = (n + block - 1) // block
+    mask = rng.random((nb, nb)) < 0.45
+    mask[2, :] = False                       # block row 2: rows 8..11 keep nothing
+    o, lse = attention_forward_head(q, k, v, 0.6, causal, None, mask, block)
+    ro, rl = _sparse_rows_loop(q, k, v, 0.6, causal, mask, block)
+    np.testing.assert_allclose(o, ro, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(np.isinf(lse), np.isinf(rl))
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(lse[fin], rl[fin], rtol=1e-12)
+    assert np.all(o[8:12] == 0.0) and np.all(np.isneginf(lse[8:12]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_finite_differences(causal):
+    rng = _rng(80 + causal)
+    n, d, block = 9, 3, 3
+    q, k, v, do = (_rand(rng, n, d) for _ in range(4))
+    mask = np.array([[1, 0, 1], [0, 1, 0], [1, 1, 0]], dtype=bool)
+    mask_empty = mask.copy()
+    mask_empty[1] = False                    # rows 3..5 attend to nothing
+
+    for m in (mask, mask_empty):
+        def loss(qq, kk, vv):
+            o, _ = attention_forward_head(qq, kk, vv, 0.5, causal, None, m, block)
+            return float((o * do).sum())
+
+        dq, dk, dv, _ = attention_backward_head(q, k, v, do, 0.5, causal, m, block)
+        h = 1e-5
+        for which, grad in ((0, dq), (1, dk), (2, dv)):
+            fd = np.zeros_like(grad)
+            for idx in np.ndindex(*grad.shape):
+                ap = [q.copy(), k.copy(), v.copy()]
+                am = [q.copy(), k.copy(), v.copy()]
+                ap[which][idx] += h
+                am[which][idx] -= h
+                fd[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+            err = np.abs(fd - grad).max() / max(np.abs(grad).max(), 1e-30)
+            assert err < 1e-7, (which, err)
+    _, _, _, D = attention_backward_head(q, k, v, do, 0.5, causal, mask_empty, block)
+    dq, _, _, _ = attention_backward_head(q, k, v, do, 0.5, causal, mask_empty, block)
+    assert np.all(dq[3:6] == 0.0) and np.all(D[3:6] == 0.0)
+
+
+def test_block_sparse_all_ones_is_dense():
+    rng = _rng(90)
+    q, k, v, do = (_rand(rng, 2, 2, 40, 6) for _ in range(4))
+    ones = np.ones((3, 3), dtype=bool)
+    for causal in (False, True):
+        a = attention_forward(q, k, v, 0.4, causal)
+        b = attention_forward(q, k, v, 0.4, causal, ones, 16)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+        ga = attention_backward(q, k, v, do, 0.4, causal)
+        gb = attention_backward(q, k, v, do, 0.4, causal, ones, 16)
+        for x, y in zip(ga, gb):
+            np.testing.assert_array_equal(x, y)
