@@ -17,6 +17,9 @@ __all__ = [
     "AttnError", "lib", "lib_path",
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
+    "attn_fwd_gqa", "attn_bwd_gqa", "attn_bwd_gqa_workspace_size",
+    "attn_fwd_sparse", "attn_bwd_sparse", "attn_fwd_sparse_workspace_size",
+    "attn_bwd_sparse_workspace_size",
     "attn_mat_fwd", "attn_mat_bwd", "attn_mat_workspace_size",
     "attn_gemm_bf16", "attn_status", "attn_strerror", "attn_version",
     "forward", "backward",
