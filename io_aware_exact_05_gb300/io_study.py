@@ -1,0 +1,149 @@
+"""IO study of the attention backward: memory traffic of the tiled (fused)
+backward against the materialise-P backward, over sequence length n and
+head dim d.
+
+"On the fine-grained I/O complexity of attention backward passes"
+(Theorem 1.1) bounds the backward's IO with a cache of M words by
+Theta(min{(n^2 d^2 + n d^3) / M, (n^2 d + n d^2) / sqrt(M)}), the first term
+for M = Omega(d^2), where tiling as FlashAttention does is optimal; the
+materialise-P backward (the small-cache algorithm's explicit n x n
+matrices) moves Theta(n^2) words through memory whatever M is.
+
+Two levels are measured, per kernel launch, with the GPU's counters:
+  * DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum), and
+  * L2 <-> SM bytes (lts__t_bytes.sum: every byte the SMs read from or write
+    to L2), the traffic between the SMs' on-chip memory (shared memory and
+    tensor memory, the "cache" of the theorem) and the memory beneath it.
+
+Run one path and configuration per process under ncu, then summarise:
+
+    ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,lts__t_bytes.sum \\
+        --clock-control none --csv --log-file io_fused_n4096_d128.csv \\
+        python -m io_aware_exact_05_gb300.io_study run --path fused --n 4096 --d 128
+    (same with --path mat into io_mat_n4096_d128.csv)
+    python -m io_aware_exact_05_gb300.io_study summarize io_*.csv
+
+`run` does one forward and one backward of the path on B=1, H=4 synthetic
+heads, non-causal.  `summarize` sums the backward launches of each file
+(fused: every launch after the forward kernel; materialise-P: every launch
+after its three forward launches) and prints bytes per path with reference
+counts: the compulsory bytes and n^2 d^2 / M with M the K, V tile a CTA keeps
+on chip.
+"""
+
+import argparse
+import csv
+import re
+import sys
+
+__all__ = ["main"]
+
+B, H = 1, 4
+
+
+def _run(path, n, d):
+    import torch
+
+    from . import attn
+    from .inputs import Workload, make_inputs
+
+    w = Workload("io", B, H, n, d, "bf16", False, 1.0, 2000 + n + d)
+    x = make_inputs(w)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (x[t].to(dev) for t in ("q", "k", "v", "do"))
+    if path == "fused":   # tiled forward, then the tiled backward (key-tile kernel + dQ)
+        o, lse = attn.forward(q, k, v)
+        attn.backward(q, k, v, o, do, lse)
+    else:                 # materialise-P: S, P, dP, dS as n x n matrices in HBM
+        ws = torch.empty(attn.attn_mat_workspace_size(B, H, n, d), dtype=torch.uint8,
+                         device=dev)
+        o, lse = torch.empty_like(q), torch.empty(B, H, n, device=dev)
+        attn.attn_mat_fwd(q, k, v, o, lse, w.scale, False, ws)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        attn.attn_mat_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, False, ws)
+    torch.cuda.synchronize()
+    rc = attn.attn_status()
+    if rc:
+        raise SystemExit("device status %d" % rc)
+
+
+def _rows(path):
+    rows = list(csv.reader(open(path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    h = rows[hi]
+    ki, mi, ui, vi = (h.index("Kernel Name"), h.index("Metric Name"), h.index("Metric Unit"),
+                      h.index("Metric Value"))
+    idi = h.index("ID")
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    launches = {}
+    for r in rows[hi + 1:]:
+        if len(r) <= vi:
+            continue
+        key = int(r[idi])
+        name = r[ki].split("(")[0].split("<")[0].split("::")[-1].split()[-1]
+        ent = launches.setdefault(key, {"name": name})
+        ent[r[mi]] = float(r[vi].replace(",", "")) * scale.get(r[ui], 1)
+    return [launches[k] for k in sorted(launches)]
+
+
+def _bwd_bytes(path):
+    """(DRAM bytes, L2 <-> SM bytes) summed over the backward launches."""
+    ls = _rows(path)
+    if "_fused_" in path:   # forward = fwd_tc_kernel, then the backward kernels
+        first = next(i for i, l in enumerate(ls) if l["name"] == "fwd_tc_kernel") + 1
+    else:                   # forward = S GEMM, row softmax, PV GEMM
+        first = 3
+    bwd = ls[first:]
+    dram = sum(l.get("dram__bytes_read.sum", 0.0) + l.get("dram__bytes_write.sum", 0.0)
+               for l in bwd)
+    return dram, sum(l.get("lts__t_bytes.sum", 0.0) for l in bwd), [l["name"] for l in bwd]
+
+
+def _summarize(paths):
+    out = []
+    for p in paths:
+        if "_fused_" not in p:
+            continue
+        m = re.search(r"n(\d+)_d(\d+)", p)
+        n, d = int(m.group(1)), int(m.group(2))
+        fd, fl, _ = _bwd_bytes(p)
+        mp = p.replace("_fused_", "_mat_")
+        md, ml = (float("nan"), float("nan"))
+        if mp in paths:
+            md, ml, _ = _bwd_bytes(mp)
+        row = {"n": n, "d": d, "fused_dram": fd, "fused_l2": fl, "mat_dram": md, "mat_l2": ml}
+        elt = 2
+        row["compulsory"] = B * H * (7 * n * d * elt + 2 * n * 4 + 2 * n * d * elt)
+        bnk, bm = 128, (64 if d == 256 else 128)
+        row["tile_m"] = bnk * d * 2            # K and V tiles resident per CTA (elements)
+        row["n2d2_over_m"] = B * H * n * n * d * d / row["tile_m"] * elt
+        out.append(row)
+    out.sort(key=lambda r: (r["d"], r["n"]))
+    print("| n | d | fused DRAM MB | fused L2<->SM MB | mat-P DRAM MB | mat-P L2<->SM MB | "
+          "compulsory MB | n^2 d^2 / M MB (M = K,V tile) | fused L2 / (n^2 d^2 / M) |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for r in out:
+        print("| %d | %d | %.1f | %.1f | %.1f | %.1f | %.1f | %.1f | %.2f |" % (
+            r["n"], r["d"], r["fused_dram"] / 1e6, r["fused_l2"] / 1e6, r["mat_dram"] / 1e6,
+            r["mat_l2"] / 1e6, r["compulsory"] / 1e6, r["n2d2_over_m"] / 1e6,
+            r["fused_l2"] / r["n2d2_over_m"]))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    sub = ap.add_subparsers(dest="cmd", required=True)
+    r = sub.add_parser("run")
+    r.add_argument("--path", choices=["fused", "mat"], required=True)
+    r.add_argument("--n", type=int, required=True)
+    r.add_argument("--d", type=int, required=True)
+    s = sub.add_parser("summarize")
+    s.add_argument("csv", nargs="+")
+    a = ap.parse_args(argv)
+    if a.cmd == "run":
+        _run(a.path, a.n, a.d)
+    else:
+        _summarize(a.csv)
+
+
+if __name__ == "__main__":
+    main(sys.argv[1:])

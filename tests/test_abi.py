@@ -187,3 +187,33 @@ def test_kept_entries_counts_the_pattern():
         j = np.arange(n)[None, :]
         keep = m[i // 128, j // 128] & ((j <= i) if causal else True)
         assert kept_entries(m, n, causal) == int(keep.sum())
+
+
+def test_io_study_summary_sums_backward_launches(tmp_path, capsys):
+    # two synthetic ncu CSVs: the fused file's backward is every launch after
+    # fwd_tc_kernel, the materialise file's every launch after three
+    from io_aware_exact_05_gb300 import io_study
+
+    hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",' \
+          '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",' \
+          '"Metric Value"\n'
+
+    def write(path, launches):
+        with open(path, "w") as f:
+            f.write(hdr)
+            for i, (name, dr, dw, l2) in enumerate(launches):
+                for m, v in (("dram__bytes_read.sum", dr), ("dram__bytes_write.sum", dw),
+                             ("lts__t_bytes.sum", l2)):
+                    f.write('"%d","1","p","h","void unnamed>::%s<1, 2>(int)","1","7","(1, 1, 1)",'
+                            '"(1, 1, 1)","0","10.3","","%s","byte","%d"\n' % (i, name, m, v))
+
+    fused = tmp_path / "io_fused_n2048_d64.csv"
+    mat = tmp_path / "io_mat_n2048_d64.csv"
+    write(fused, [("fwd_tc_kernel", 7, 7, 7), ("delta_kernel", 1, 2, 30), ("bwd_kv_kernel", 3, 4, 50)])
+    write(mat, [("gemm_bf16_kernel", 9, 9, 9), ("mat_softmax_kernel", 9, 9, 9),
+                ("gemm_bf16_kernel", 9, 9, 9), ("gemm_bf16_kernel", 5e6, 5e6, 1e7)])
+    io_study.main(["summarize", str(fused), str(mat)])
+    line = [l for l in capsys.readouterr().out.splitlines() if l.startswith("| 2048 |")][0]
+    cells = [c.strip() for c in line.strip("|").split("|")]
+    assert cells[2] == "0.0" and cells[3] == "0.0"        # 10 bytes, 80 bytes in MB
+    assert cells[4] == "10.0" and cells[5] == "10.0"      # materialise backward: 1e7 bytes each
