@@ -26,6 +26,16 @@ random blocks per block row, as in Longformer and BigBird):
 
   b2h16_n16k_d128_sparse  B2 H16 n16384 d128 bf16 non-causal  w 2, g 1, r 2
 
+FP8 workloads (forward only): bf16 draws that the FP8 path quantises to
+e4m3 itself (per-head scales, V transposed); the outlier variant adds to each
+entry of Q and K, with probability 1e-3, an extra N(0, 10^2) draw (a few
+large activations, the case incoherent processing is for):
+
+  b2h16_n8k_d128_fp8           B2 H16 n8192 d128 causal  N(0,1)
+  b1h4_n4k_d128_fp8_outliers   B1 H4  n4096 d128 causal  N(0,1) + outliers on Q, K
+
+make_signs draws the random signs of the incoherent-processing rotation.
+
 Values are drawn in float32 and rounded to bf16 round-to-nearest-even; the
 Q/K factor 2.0 of the sharp-softmax workload is a power of two, so it is
 exact in either dtype.
@@ -35,8 +45,8 @@ from dataclasses import dataclass, replace
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "GQA_WORKLOADS", "SPARSE_WORKLOADS", "workload",
-           "make_inputs", "make_block_mask"]
+__all__ = ["Workload", "WORKLOADS", "GQA_WORKLOADS", "SPARSE_WORKLOADS", "FP8_WORKLOADS",
+           "workload", "make_inputs", "make_signs", "make_block_mask"]
 
 
 @dataclass(frozen=True)
@@ -52,6 +62,8 @@ class Workload:
     seed: int = 0
     H_kv: int = 0       # key/value heads; 0 means one per query head (H)
     sparse: tuple = ()  # (window, global, random) blocks of a block mask; () = dense
+    fp8: bool = False   # forward-only e4m3 workload (quantised by the FP8 path)
+    outliers: tuple = ()  # (probability, std) of an extra Gaussian on Q, K entries
 
     @property
     def kv_heads(self):
@@ -91,8 +103,15 @@ SPARSE_WORKLOADS = [
 ]
 
 
+FP8_WORKLOADS = [
+    Workload("b2h16_n8k_d128_fp8", 2, 16, 8192, 128, "bf16", True, 1.0, 1003, fp8=True),
+    Workload("b1h4_n4k_d128_fp8_outliers", 1, 4, 4096, 128, "bf16", True, 1.0, 1009, fp8=True,
+             outliers=(1e-3, 10.0)),
+]
+
+
 def workload(name):
-    for w in WORKLOADS + GQA_WORKLOADS + SPARSE_WORKLOADS:
+    for w in WORKLOADS + GQA_WORKLOADS + SPARSE_WORKLOADS + FP8_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
@@ -102,15 +121,25 @@ def make_inputs(w, device="cpu", pin=False):
     """Draw q, do of shape (B, H, n, d) and k, v of shape (B, H_kv, n, d)
     for workload ``w``.
 
-    Draw order is fixed (q, k, v, do) from ``torch.Generator().manual_seed(w.seed)``.
+    Draw order is fixed (q, k, v, do) from ``torch.Generator().manual_seed(w.seed)``,
+    then, for an outlier workload, the outlier mask and values of q and of k.
     Returns a dict of tensors in ``w.torch_dtype`` on ``device`` (pinned host
     memory if ``pin`` and device is cpu).
     """
     g = torch.Generator(device="cpu").manual_seed(int(w.seed))
-    out = {}
+    raw = {}
     for name in ("q", "k", "v", "do"):
         heads = w.kv_heads if name in ("k", "v") else w.H
-        x = torch.randn((w.B, heads, w.n, w.d), generator=g, dtype=torch.float32)
+        raw[name] = torch.randn((w.B, heads, w.n, w.d), generator=g, dtype=torch.float32)
+    if w.outliers:
+        prob, std = w.outliers
+        for name in ("q", "k"):
+            hit = torch.rand(raw[name].shape, generator=g) < prob
+            extra = torch.randn(raw[name].shape, generator=g) * std
+            raw[name] = raw[name] + hit * extra
+    out = {}
+    for name in ("q", "k", "v", "do"):
+        x = raw[name]
         if name in ("q", "k") and w.qk_gain != 1.0:
             x.mul_(w.qk_gain)
         x = x.to(w.torch_dtype)
@@ -136,3 +165,10 @@ def make_block_mask(n, window, n_global, n_random, seed, block=128):
             pick = torch.randperm(nb, generator=g)[:min(n_random, nb)]
             m[row, pick] = True
     return m.to(torch.uint8)
+
+
+def make_signs(d, seed):
+    """d random signs (+1.0 / -1.0, float32) for the incoherent-processing
+    rotation, from ``torch.Generator().manual_seed(seed)``."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    return torch.randint(0, 2, (d,), generator=g).float() * 2.0 - 1.0

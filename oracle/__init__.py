@@ -8,6 +8,7 @@ Every function is pinned by tests/test_oracle.py (no function here is
 "parity unpinned").
 """
 
+from . import fp8  # noqa: F401
 from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_head,
