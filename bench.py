@@ -37,6 +37,8 @@ from io_aware_exact_05_gb300.flops import (attention_flops, kept_entries,  # noq
 from io_aware_exact_05_gb300.inputs import make_block_mask, make_inputs, workload  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+METRIC_FP8 = ("attention fwd TFLOP/s with e4m3 Q/K/V/P (bf16 inputs quantised on device), "
+              "1×GB300")
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "b2h16_n8k_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -116,9 +118,17 @@ def block_mask_of(w):
     return make_block_mask(w.n, *w.sparse, w.seed) if w.sparse else None
 
 
+def metric_of(w):
+    return METRIC_FP8 if w.fp8 else METRIC
+
+
 def step_flops(w, n=None):
-    """Algorithmic FLOPs of one forward + backward of w (on its first n tokens)."""
+    """Algorithmic FLOPs of one step of w (on its first n tokens): forward +
+    backward, or the forward alone for an e4m3 workload."""
     n = w.n if n is None else n
+    if w.fp8:
+        f = attention_flops(w.B, w.H, n, w.d, w.causal)
+        return {"fwd": f["fwd"], "bwd": 0, "total": f["fwd"]}
     if w.sparse:
         nb = (n + 127) // 128
         kept = kept_entries(block_mask_of(w).numpy()[:nb, :nb], n, w.causal)
@@ -128,19 +138,28 @@ def step_flops(w, n=None):
 
 def oracle_step(w, x, heads, n_sub=None):
     """Float64 CPU oracle forward + backward over the given heads, on the
-    first n_sub tokens of each (the whole head by default)."""
+    first n_sub tokens of each (the whole head by default).  For an e4m3
+    workload: per-head e4m3 quantisation of q, k, v, then the forward of the
+    values the codes stand for."""
     import oracle
+    from oracle import fp8
 
     m = w.n if n_sub is None else n_sub
     bm = block_mask_of(w)
     bm = None if bm is None else bm.numpy().astype(bool)[:(m + 127) // 128, :(m + 127) // 128]
-    q, do = (x[n].reshape(w.B * w.H, w.n, w.d) for n in ("q", "do"))
+    q = x["q"].reshape(w.B * w.H, w.n, w.d)
     k, v = (x[n].reshape(w.B * w.kv_heads, w.n, w.d) for n in ("k", "v"))
     g = w.H // w.kv_heads
     for h in heads:
         hk = (h // w.H) * w.kv_heads + (h % w.H) // g   # key/value head of query head h
+        if w.fp8:
+            ops = [fp8.dequantize(*fp8.quantize_per_head(t[:m].double().numpy())[:2])
+                   for t in (q[h], k[hk], v[hk])]
+            oracle.attention_forward_head(*ops, w.scale, w.causal)
+            continue
         oracle.attention_forward_head(q[h][:m], k[hk][:m], v[hk][:m], w.scale, w.causal,
                                       None, bm)
+        do = x["do"].reshape(w.B * w.H, w.n, w.d)
         oracle.attention_backward_head(q[h][:m], k[hk][:m], v[hk][:m], do[h][:m], w.scale,
                                        w.causal, bm)
 
@@ -164,8 +183,10 @@ def time_oracle(w, x, budget_s=12.0, max_heads=4):
             break
     f = step_flops(w)["total"] * len(heads) // (w.B * w.H)
     return {"value": f / t / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": "float64 numpy oracle, forward+backward of %d of %d whole heads of %s "
-                      "(%.1f s)" % (len(heads), w.B * w.H, w.name, t)}
+            "sample": "float64 numpy oracle, %s of %d of %d whole heads of %s "
+                      "(%.1f s)" % ("e4m3 quantisation + forward" if w.fp8
+                                    else "forward+backward", len(heads),
+                                    w.B * w.H, w.name, t)}
 
 
 def run_reference(args, w):
@@ -191,9 +212,11 @@ def run_reference(args, w):
         oracle_step(w, x, [s % (w.B * w.H)], n_sub)
     el = time.perf_counter() - t0
     val = per_step * args.steps / el / 1e12
-    sample = ("forward+backward of the first %d of %d tokens of one head (d=%d, %s) per step, "
-              "float64 numpy oracle" % (n_sub, w.n, w.d, "causal" if w.causal else "full"))
-    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+    sample = ("%s of the first %d of %d tokens of one head (d=%d, %s) per step, "
+              "float64 numpy oracle" % ("e4m3 quantisation + forward" if w.fp8
+                                        else "forward+backward", n_sub, w.n,
+                                        w.d, "causal" if w.causal else "full"))
+    line = {"metric": metric_of(w), "value": val, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
@@ -302,10 +325,12 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    n_launch0 = attn.attn_launch_count()
     t0.record(st)
     for i in range(args.steps):
         step(ev[i])
     t1.record(st)
+    launches = attn.attn_launch_count() - n_launch0
     torch.cuda.synchronize()
     if dist:
         tdist.barrier()
@@ -394,7 +419,157 @@ def run_ours(args, w):
                              src, pk.get("bf16_tflops_sustained"))},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and ws_n == 1:
+            line["cpu_baseline"] = time_oracle(w, x)
+        print(json.dumps(line), flush=True)
+    if dist:
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+def run_fp8(args, w):
+    """One step = per-head e4m3 quantisation of the bf16 Q, K, V on the device
+    (attn_quantize_fp8, V transposed) and one FP8 forward (attn_fwd_fp8)."""
+    from io_aware_exact_05_gb300 import attn
+
+    ws_n, rank, local = dist_env()
+    dist = ws_n > 1
+    if dist:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wr = w.with_shape(seed=w.seed + 7919 * rank)    # each rank its own batch
+    x = make_inputs(wr)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    BH = w.B * w.H
+    q8 = torch.empty(w.B, w.H, w.n, w.d, dtype=torch.float8_e4m3fn, device=dev)
+    k8 = torch.empty_like(q8)
+    vt8 = torch.empty(w.B, w.H, w.d, w.n, dtype=torch.float8_e4m3fn, device=dev)
+    ds = [torch.empty(w.B, w.H, dtype=torch.float32, device=dev) for _ in range(3)]
+    qws = torch.empty(max(4, attn.attn_quantize_fp8_workspace_size(BH, w.n, w.d)),
+                      dtype=torch.uint8, device=dev)
+    o = torch.empty(w.B, w.H, w.n, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e: e[0].record(st)
+        attn.attn_quantize_fp8(q, q8, ds[0], False, None, qws, st)
+        attn.attn_quantize_fp8(k, k8, ds[1], False, None, qws, st)
+        attn.attn_quantize_fp8(v, vt8, ds[2], True, None, qws, st)
+        if e: e[1].record(st)
+        attn.attn_fwd_fp8(q8, k8, vt8, o, lse, w.scale, w.causal, *ds, stream=st)
+        if e: e[2].record(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after warm-up: " + attn.attn_strerror(rc))
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    n_launch0 = attn.attn_launch_count()
+    t0.record(st)
+    for i in range(args.steps):
+        step(ev[i])
+    t1.record(st)
+    launches = attn.attn_launch_count() - n_launch0
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    clk = clocks.stop()
+    el_ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([el_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        el_ms = float(tt.item())
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after timing: " + attn.attn_strerror(rc))
+    stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(args.steps)) / args.steps
+                for s in range(2)]
+    per_step = step_flops(w)["total"]
+    value = per_step * ws_n * args.steps / (el_ms * 1e-3) / 1e12
+
+    # ---- end to end: bf16 inputs from pinned host memory, O and LSE back
+    hx = {n: x[n].pin_memory() for n in ("q", "k", "v")}
+    dx = {"q": q, "k": k, "v": v}
+    ho = {"o": torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+          "lse": torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        for n_, t in hx.items():
+            dx[n_].copy_(t, non_blocking=True)
+        step()
+        ho["o"].copy_(o, non_blocking=True)
+        ho["lse"].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        pk, src = peaks()
+        # dense e4m3 peak: the measured bf16 peak x the nominal e4m3 / bf16
+        # ratio (4.5 / 2.25 PFLOP/s)
+        peak = 2.0 * float(pk["bf16_tflops"])
+        achieved = per_step / (stage_ms[1] * 1e-3) / 1e12
+        # quantiser: 2 bytes read + 1 byte written per element of Q, K, V
+        q_bytes = 3 * BH * w.n * w.d * 3
+        q_gbs = q_bytes / (stage_ms[0] * 1e-3) / 1e9
+        line = {
+            "metric": METRIC_FP8, "value": value, "unit": UNIT, "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "pct_of_peak": 100.0 * value / ws_n / peak,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
+                       "causal": w.causal,
+                       "quantisation": "per-head amax/448 on device, V as [d][n], no rotation",
+                       "parallelism": "replicas x%d (heads independent)" % ws_n,
+                       "l2": "inputs larger than L2: Q,K,V bf16 = %.0f MB per GPU vs 126 MB L2"
+                             % (h2d / 1e6)},
+            "stage_ms": {"quantize_qkv": stage_ms[0], "fwd_fp8": stage_ms[1]},
+            "tflops": {"fwd_fp8_kernel": achieved},
+            "roofline": {"kernel": "fwd_fp8_kernel (attn_fwd_fp8)", "bound": "tensor",
+                         "flops_per_launch": per_step, "achieved": achieved, "peak": peak,
+                         "unit": UNIT, "frac": achieved / peak, "traffic": None,
+                         "peak_source": "%s bf16_tflops (burst) x 2 (nominal e4m3/bf16)" % src},
+            "quantize_roofline": {"bound": "hbm", "bytes_per_step": q_bytes, "achieved": q_gbs,
+                                  "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                                  "frac": q_gbs / float(pk["hbm_gbs"])},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches,
             "clocks": clk,
         }
         if not args.no_cpu_baseline and ws_n == 1:
@@ -418,6 +593,8 @@ def main():
     w = workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.fp8:
+        run_fp8(args, w)
     else:
         run_ours(args, w)
 

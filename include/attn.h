@@ -33,7 +33,8 @@
  *     on the device (a bounded wait that ran out) are recorded in a device
  *     status word read by attn_status().
  *   - bf16 path: d in {64, 128, 256}; fp32 path: 1 <= d <= 256.  Any n >= 1.
- *   - Thread-safe: the only global state is the device status word.
+ *   - Thread-safe: the only global state is the device status word, the
+ *     fixed scratch of attn_bwd_noalloc and an atomic launch counter.
  */
 #ifndef ATTN_H
 #define ATTN_H
@@ -136,6 +137,57 @@ ATTN_API int attn_bwd(const void* Q, const void* K, const void* V, const void* O
 ATTN_API int attn_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           int B, int H, int H_kv, int n, int d, attn_dtype dtype, float scale,
                           int causal, void* stream);
+/*
+ * attn_fwd_fp8 -- forward pass with FP8 (e4m3) operands on the FP8 tensor
+ * cores ("Flash Attention: Revolutionizing Transformer Efficiency", section
+ * FlashAttention-3, item 2: FP8 computation).  Head dim 128 only; n a
+ * multiple of 16 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   Q8, K8 : DEVICE e4m3 bytes [B][H][n][128]
+ *   Vt8    : DEVICE e4m3 bytes [B][H][128][n]  (V transposed: every FP8
+ *            operand of the tensor cores is then K-major)
+ *   O      : output bf16 [B][H][n][128];  LSE : output fp32 [B][H][n]
+ *   descale_q, descale_k, descale_v : DEVICE fp32 [B*H] per-head scales
+ *            (real value = descale x e4m3 value), or NULL for 1; as written
+ *            by attn_quantize_fp8.  4-byte aligned.
+ * Computes softmax(scale * dq[h] * dk[h] * Q8 K8^T) (dv[h] V8) with fp32
+ * accumulation; the probabilities P are rounded to e4m3 before the P V
+ * product, while the row sums use the unrounded fp32 values, so
+ * O - O_ref = sum_j (e4m3(p_j) - p_j) v_j / l.  Each rounding is at most
+ * 2^-4 of p_j (P <= 2^8 by the running-maximum rule, inside e4m3's range)
+ * and, for random inputs, unbiased, which puts the RMS of O - O_ref near
+ * 0.027 of the RMS of O_ref (the RMS relative rounding error of e4m3).
+ * Tested against the exact result on the same e4m3 inputs: RMS ratio
+ * <= 0.035, max|O - O_ref| <= 0.08 max|O_ref|, LSE to 1e-5 relative.
+ */
+ATTN_API int attn_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, float* LSE,
+                          int B, int H, int n, int d, float scale, const float* descale_q,
+                          const float* descale_k, const float* descale_v, int causal,
+                          void* stream);
+
+/*
+ * attn_quantize_fp8 -- per-head e4m3 encoding of a bf16 attention operand
+ * for attn_fwd_fp8, with the optional rotation of incoherent processing
+ * ("Flash Attention: Revolutionizing Transformer Efficiency", section
+ * FlashAttention-3, items 2 and 3).
+ *   X        : DEVICE bf16 [BH][n][d], d = 128 (ATTN_ERR_UNSUPPORTED else)
+ *   X8       : DEVICE output e4m3 bytes, [BH][n][128], or [BH][128][n] when
+ *              transpose = 1 (for V; n must then be a multiple of 16)
+ *   descale  : DEVICE output fp32 [BH]: amax_h / 448 (1 for a zero head)
+ *   signs    : DEVICE fp32 [128] of +1 / -1, or NULL.  When given, each row
+ *              x is replaced by x diag(signs) H_128 / sqrt(128) (H the
+ *              Sylvester Hadamard matrix) before encoding; use the same
+ *              signs for Q and K (their scores are unchanged) and none for V
+ *              (transpose with signs is ATTN_ERR_INVALID_ARG).
+ *   workspace: DEVICE scratch of attn_quantize_fp8_workspace_size bytes.
+ * codes = round-to-nearest-even e4m3 of y * (448 / amax_h), saturating at
+ * 448.  X, X8 16-byte aligned; descale, signs, workspace 4-byte aligned.
+ * Two kernels (head maximum, then codes); no synchronisation.
+ */
+ATTN_API size_t attn_quantize_fp8_workspace_size(int BH, int n, int d);
+ATTN_API int attn_quantize_fp8(const void* X, void* X8, float* descale, int BH, int n, int d,
+                               int transpose, const float* signs, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /*
  * Block-sparse exact attention.  A block pattern keeps or drops 128 x 128
  * blocks of the score matrix: block_mask is a DEVICE uint8 array
@@ -276,6 +328,12 @@ ATTN_API int attn_gemm_bf16(const void* A, const void* Bm, void* C, int batch, i
 /* Synchronises `stream`, then returns and clears the first device-side
  * error recorded since the last call (ATTN_OK if none). */
 ATTN_API int attn_status(void* stream);
+
+/* Number of kernels the library has enqueued in this process so far
+ * (every launch by every entry point, counted on the host when it is
+ * issued).  The difference across a region is how many of the library's
+ * kernels that region launched. */
+ATTN_API unsigned long long attn_launch_count(void);
 
 /* Static description of a status code. */
 ATTN_API const char* attn_strerror(int code);

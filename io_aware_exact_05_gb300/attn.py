@@ -18,10 +18,11 @@ __all__ = [
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
     "attn_fwd_gqa", "attn_bwd_gqa", "attn_bwd_gqa_workspace_size",
-    "attn_fwd_sparse", "attn_bwd_sparse", "attn_fwd_sparse_workspace_size",
+    "attn_fwd_sparse", "attn_bwd_sparse", "attn_fwd_sparse_workspace_size", "attn_fwd_fp8",
+    "forward_fp8", "attn_quantize_fp8", "attn_quantize_fp8_workspace_size", "quantize_fp8",
     "attn_bwd_sparse_workspace_size",
     "attn_mat_fwd", "attn_mat_bwd", "attn_mat_workspace_size",
-    "attn_gemm_bf16", "attn_status", "attn_strerror", "attn_version",
+    "attn_gemm_bf16", "attn_status", "attn_strerror", "attn_version", "attn_launch_count",
     "forward", "backward",
 ]
 
@@ -67,6 +68,12 @@ def lib():
             L.attn_bwd_gqa.restype = i
             L.attn_bwd_gqa_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
             L.attn_bwd_gqa_workspace_size.restype = sz
+            L.attn_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, vp, vp, vp, i, vp]
+            L.attn_fwd_fp8.restype = i
+            L.attn_quantize_fp8_workspace_size.argtypes = [i, i, i]
+            L.attn_quantize_fp8_workspace_size.restype = sz
+            L.attn_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, vp, vp, sz, vp]
+            L.attn_quantize_fp8.restype = i
             L.attn_fwd_sparse_workspace_size.argtypes = [i, i]
             L.attn_fwd_sparse_workspace_size.restype = sz
             L.attn_fwd_sparse.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, vp, vp, sz, vp]
@@ -94,6 +101,8 @@ def lib():
             L.attn_strerror.argtypes = [i]
             L.attn_strerror.restype = ctypes.c_char_p
             L.attn_version.argtypes = []
+            L.attn_launch_count.argtypes = []
+            L.attn_launch_count.restype = ctypes.c_ulonglong
             L.attn_version.restype = ctypes.c_char_p
             _LIB = L
     return _LIB
@@ -139,6 +148,11 @@ def attn_version():
 def attn_status(stream=None):
     """Synchronise the stream; return and clear the first device-side error."""
     return lib().attn_status(_stream(stream))
+
+
+def attn_launch_count():
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().attn_launch_count())
 
 
 def attn_fwd(Q, K, V, O, LSE, scale, causal, stream=None):
@@ -202,6 +216,56 @@ def attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AU
                             int(bool(causal)), int(mode), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_bwd_gqa")
+
+
+def attn_fwd_fp8(Q8, K8, Vt8, O, LSE, scale, causal, descale_q=None, descale_k=None,
+                 descale_v=None, stream=None):
+    """FP8 forward: Q8, K8 [B, H, n, 128] and Vt8 [B, H, 128, n] e4m3 tensors,
+    per-head fp32 descales [B, H] on the device (None = 1), O bf16, LSE fp32."""
+    B, H, n, d = _shape(Q8)
+    rc = lib().attn_fwd_fp8(_ptr(Q8), _ptr(K8), _ptr(Vt8), _ptr(O), _ptr(LSE), B, H, n, d,
+                            float(scale), _ptr(descale_q), _ptr(descale_k), _ptr(descale_v),
+                            int(bool(causal)), _stream(stream))
+    _check(rc, "attn_fwd_fp8")
+
+
+def attn_quantize_fp8_workspace_size(BH, n, d):
+    return int(lib().attn_quantize_fp8_workspace_size(int(BH), int(n), int(d)))
+
+
+def attn_quantize_fp8(X, X8, descale, transpose=False, signs=None, workspace=None, stream=None):
+    """Per-head e4m3 encoding of X bf16 [B, H, n, 128] into X8 (same shape, or
+    [B, H, 128, n] when transposed) and descale [B, H]; signs (128 floats of
+    +-1) selects the Hadamard rotation of incoherent processing."""
+    B, H, n, d = _shape(X)
+    if workspace is None:
+        workspace = torch.empty(max(attn_quantize_fp8_workspace_size(B * H, n, d), 4),
+                                dtype=torch.uint8, device=X.device)
+    rc = lib().attn_quantize_fp8(_ptr(X), _ptr(X8), _ptr(descale), B * H, n, d,
+                                 int(bool(transpose)), _ptr(signs), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_quantize_fp8")
+
+
+def quantize_fp8(x, transpose=False, signs=None, stream=None):
+    """Allocate and run attn_quantize_fp8.  Returns (x8, descale)."""
+    B, H, n, d = _shape(x)
+    shape = (B, H, d, n) if transpose else (B, H, n, d)
+    x8 = torch.empty(shape, dtype=torch.float8_e4m3fn, device=x.device)
+    descale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    attn_quantize_fp8(x, x8, descale, transpose, signs, None, stream)
+    return x8, descale
+
+
+def forward_fp8(q8, k8, vt8, descales=(None, None, None), causal=False, scale=None,
+                stream=None):
+    """Allocate O (bf16) and LSE and run attn_fwd_fp8.  Returns (O, LSE)."""
+    B, H, n, d = _shape(q8)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty((B, H, n, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device=q8.device)
+    attn_fwd_fp8(q8, k8, vt8, o, lse, scale, causal, *descales, stream=stream)
+    return o, lse
 
 
 def attn_fwd_sparse_workspace_size(n, d):

@@ -259,6 +259,42 @@ static bool ptrs_ok(std::initializer_list<const void*> ps) {
   return true;
 }
 
+int attn_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, float* LSE, int B,
+                 int H, int n, int d, float scale, const float* descale_q,
+                 const float* descale_k, const float* descale_v, int causal, void* stream) {
+  if (!ptrs_ok({Q8, K8, Vt8, O, LSE})) return ATTN_ERR_INVALID_ARG;
+  for (const float* p : {descale_q, descale_k, descale_v})
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return ATTN_ERR_INVALID_ARG;
+  int rc = check_common(B, H, n, d, scale, causal);
+  if (rc) return rc;
+  if (d != 128 || n % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  return launch_fwd_fp8(Q8, K8, Vt8, O, LSE, B * H, n, scale, descale_q, descale_k, descale_v,
+                        causal, default_ctl(), static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_quantize_fp8_workspace_size(int BH, int n, int d) {
+  if (BH < 1 || n < 1 || d != 128) return 0;
+  return quant_fp8_workspace_bytes(BH, n);
+}
+
+int attn_quantize_fp8(const void* X, void* X8, float* descale, int BH, int n, int d,
+                      int transpose, const float* signs, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (!ptrs_ok({X, X8}) || !descale || (reinterpret_cast<uintptr_t>(descale) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (BH < 1 || n < 1 || d < 1 || (transpose != 0 && transpose != 1)) return ATTN_ERR_INVALID_ARG;
+  if (transpose && signs) return ATTN_ERR_INVALID_ARG;   // V is never rotated
+  if (BH > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 || (transpose && n % 16 != 0)) return ATTN_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 3u) ||
+      workspace_bytes < quant_fp8_workspace_bytes(BH, n))
+    return ATTN_ERR_WORKSPACE;
+  return cuda_rc(launch_quant_fp8(X, X8, descale, BH, n, transpose != 0, signs,
+                                  static_cast<float*>(workspace),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
 int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, int H, int n,
                         int d, attn_dtype dtype, int causal, attn_dq_mode mode, void* workspace,
                         size_t workspace_bytes, void* stream) {
@@ -524,6 +560,8 @@ const char* attn_strerror(int code) {
     default: return "unknown status code";
   }
 }
+
+unsigned long long attn_launch_count(void) { return attn::launch_count(); }
 
 const char* attn_version(void) { return "libattn 0.1 (sm_103a)"; }
 

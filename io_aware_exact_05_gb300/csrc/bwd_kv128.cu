@@ -485,6 +485,7 @@ int launch(const void* Q, const void* K, const void* V, const void* dO, const fl
                                               static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
                                               gsplit, tl, n, n_pad, scale,
                                               scale * 1.4426950408889634f, causal, ctl);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

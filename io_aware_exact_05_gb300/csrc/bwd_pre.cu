@@ -89,14 +89,17 @@ cudaError_t launch_delta_bf16(const void* O, const void* dO, const float* LSE, f
     case 64:
       delta_kernel<64><<<ceil_div(rows, 32), 256, 0, st>>>(o, g, LSE, Dv, LSE2, dQacc, n, n_pad,
                                                           rows);
+      note_launch();
       break;
     case 128:
       delta_kernel<128><<<ceil_div(rows, 16), 256, 0, st>>>(o, g, LSE, Dv, LSE2, dQacc, n, n_pad,
                                                            rows);
+      note_launch();
       break;
     case 256:
       delta_kernel<256><<<ceil_div(rows, 8), 256, 0, st>>>(o, g, LSE, Dv, LSE2, dQacc, n, n_pad,
                                                           rows);
+      note_launch();
       break;
     default:
       return cudaErrorInvalidValue;
@@ -109,6 +112,7 @@ cudaError_t launch_dq_convert(const float* acc, void* dQ, size_t elems, cudaStre
   if (n8 == 0) return cudaSuccess;
   dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
       acc, static_cast<__nv_bfloat16*>(dQ), n8);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -694,6 +694,7 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
                                            gsplit, tl, n, n_pad, scale,
                                            scale * 1.4426950408889634f, causal, ctl);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -716,6 +717,7 @@ int launch_q(const void* Q, const void* K, const void* V, const void* dO, const 
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, static_cast<__nv_bfloat16*>(dQ),
                                            hm, tl, n, n_pad, scale, scale * 1.4426950408889634f,
                                            causal, ctl);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

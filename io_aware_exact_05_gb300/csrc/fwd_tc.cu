@@ -329,36 +329,37 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int c = 0; c < BN; ++c)
           if (col0 + c >= lim) s[c] = -INFINITY;
       }
-      // row maximum with eight independent chains
-      float mx8[8];
+      // row maximum: three-input maxima in four independent chains
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
-#pragma unroll
-      for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 4; c < BN; c += 2) mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], s[c], s[c + 1]);
+      const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       const float m_cand = mx * scale_log2;
       const float m_new = (m_cand > m + 8.0f) ? m_cand : m;
       // SPARSE: a row can have no kept score yet (m_new = -inf); exponents are
       // then taken against 0, so P = 0 and alpha = 0 instead of NaN
       const float m_base = (SPARSE && m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2(m - m_base);   // 0 on the first tile (m = -inf)
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // exponents and row sum on column pairs (paired fp32 FMA and add)
+      const float2 c2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(-m_base, -m_base);
+      float2 rs4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[c0 + 2 * i], scale_log2, -m_base));
-          const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale_log2, -m_base));
-          rs8[(2 * i) & 7] += p0;
-          rs8[(2 * i + 1) & 7] += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
+          const float2 p = make_float2(ex2(x.x), ex2(x.y));
+          rs4[i & 3] = __fadd2_rn(rs4[i & 3], p);
+          pk[i] = pack_bf16x2(p.x, p.y);
         }
         tmem_st16(pa + c0 / 2, pk);
       }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
+      const float rs = rs2.x + rs2.y;
       tmem_st_wait();
       l = l * alpha + rs;
       // Wait for PV of tile j-1 every iteration: a parity wait is only
@@ -377,8 +378,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           uint32_t rr[32];
           tmem_ld32(oa + c0, rr);
           tmem_ld_wait();
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 o2 = __fmul2_rn(
+                make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), a2);
+            rr[i] = __float_as_uint(o2.x);
+            rr[i + 1] = __float_as_uint(o2.y);
+          }
           tmem_st32(oa + c0, rr);
         }
         tmem_st_wait();
@@ -445,6 +452,7 @@ int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE,
   const float scale_log2 = scale * 1.4426950408889634f;
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, hm, tl,
                                            n, scale_log2, causal, ctl);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

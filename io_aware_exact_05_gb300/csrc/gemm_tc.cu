@@ -200,6 +200,7 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int ba
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(N, BN), ceil_div(M, kBM), batch);
   kern<<<grid, 128, smem, st>>>(ta, tb, C, M, N, K, alpha, ctl);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -2,11 +2,19 @@
 // word shared by every kernel of the library.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
 
 namespace attn {
+
+// Kernels the library has launched in this process.
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 // First device-side error: [0] = attn_status_t code, [1] = wait site.
 __device__ int g_status_word[2];
@@ -38,6 +46,20 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, 
   const cuuint32_t box[3] = {box_x, box_y, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                  uint32_t box_x, uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {x, y, z};
+  const cuuint64_t strides[2] = {x, x * y};   // bytes, dims 1..2
+  const cuuint32_t box[3] = {box_x, box_y, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -15,12 +15,20 @@ namespace attn {
 // 128-byte swizzle and zero fill outside the tensor.  box_x * 2 must be 128.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
                     uint32_t box_x, uint32_t box_y);
+// A 3-D 8-bit tensor map over [z][y][x], 128-byte swizzle, zero fill outside
+// the tensor (box_x must be 128; x a multiple of 16).
+bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
+                  uint32_t box_x, uint32_t box_y);
 // A 3-D fp32 tensor map over [z][y][x] for reduce-add tiles; with sw128 the
 // shared-memory tile uses the 128-byte swizzle (box_x * 4 must then be 128).
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
                    uint32_t box_x, uint32_t box_y, bool sw128 = false);
 
 KernelCtl default_ctl();
+
+// Counts one kernel launch of the library (host side; attn_launch_count).
+void note_launch();
+unsigned long long launch_count();
 
 // Block-sparse tile lists (built by launch_tile_lists in sparse.cu): for
 // outer unit u, lists[u * stride + p], p < counts[u], are the inner tiles to
@@ -98,6 +106,20 @@ int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
                     const KernelCtl& ctl, cudaStream_t st);
 // Tiling of the query-tile dQ kernel (query tiles of query_rows, key tiles of kv_rows).
 void bwd_q_tiling(int d, int* query_rows, int* kv_rows);
+
+// FP8 (e4m3) forward for d = 128: Q, K [BH][n][128], Vt [BH][128][n] e4m3 bytes,
+// O bf16 [BH][n][128], LSE fp32.  n must be a multiple of 16.
+// descale_q/k/v: device arrays of BH floats, or null for 1.
+int launch_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, float* LSE, int BH,
+                   int n, float scale, const float* descale_q, const float* descale_k,
+                   const float* descale_v, int causal, const KernelCtl& ctl, cudaStream_t st);
+
+// Per-head e4m3 quantisation of X bf16 [BH][n][128] into X8 ([BH][n][128],
+// or [BH][128][n] when transpose) and descale [BH]; signs (128 floats of +-1)
+// or null selects the Hadamard rotation.  partial: quant_fp8_workspace_bytes.
+size_t quant_fp8_workspace_bytes(int BH, int n);
+cudaError_t launch_quant_fp8(const void* X, void* X8, float* descale, int BH, int n, bool transpose,
+                             const float* signs, float* partial, cudaStream_t st);
 
 // ---- block-sparse tile lists (sparse.cu) ----------------------------------------------
 size_t tile_lists_bytes(int n, int osz, int members, int isz);

@@ -115,6 +115,7 @@ cudaError_t launch_mat_softmax(const float* S, void* P, float* LSE, int BH, int 
   dim3 grid(n, BH);
   mat_softmax_kernel<<<grid, kThreads, 0, st>>>(S, static_cast<__nv_bfloat16*>(P), LSE, n,
                                                 causal);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -123,6 +124,7 @@ cudaError_t launch_mat_dsoftmax(const void* P, const float* dP, const float* Dv,
   const size_t total8 = (size_t)BH * n * n / 8;
   mat_dsoftmax_kernel<<<(unsigned)((total8 + kThreads - 1) / kThreads), kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(P), dP, Dv, static_cast<__nv_bfloat16*>(dS), n, total8);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -230,6 +230,7 @@ cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
   fwd_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, O, LSE, hm, bmask, n, d, scale,
                                                       causal);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -238,6 +239,7 @@ cudaError_t launch_delta_f32(const float* O, const float* dO, float* Dv, int BH,
   const int rows = BH * n;
   delta_f32_kernel<<<ceil_div(rows, kRowsPerBlock), kRowsPerBlock * 32, 0, st>>>(O, dO, Dv, rows,
                                                                                  d);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -248,6 +250,7 @@ cudaError_t launch_bwd_dkdv_f32(const float* Q, const float* K, const float* V, 
   dim3 grid(ceil_div(n, kRowsPerBlock), BH / hm.group);
   bwd_dkdv_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dK, dV, hm, bmask,
                                                            n, d, scale, causal);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -258,6 +261,7 @@ cudaError_t launch_bwd_dq_f32(const float* Q, const float* K, const float* V, co
   dim3 grid(ceil_div(n, kRowsPerBlock), BH);
   bwd_dq_f32_kernel<<<grid, kRowsPerBlock * 32, 0, st>>>(Q, K, V, dO, LSE, Dv, dQ, hm, bmask, n, d,
                                                          scale, causal);
+  note_launch();
   return cudaGetLastError();
 }
 

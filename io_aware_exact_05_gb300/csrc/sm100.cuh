@@ -285,6 +285,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format 0 at bits
+// [7,10) and [10,13)), fp32 accumulation, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  Start address, leading
 // byte offset and stride byte offset are stored >> 4; bit 46 is the fixed
 // descriptor version; bits [61,64) = 2 select the 128-byte swizzle.
@@ -327,7 +333,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // iff acc != 0; the other three always accumulate.  The _pair forms issue
 // the CTA-pair MMA (M = 256: A rows and B columns split between the CTAs,
 // each CTA's half at the same shared-memory and tensor-memory addresses).
-#define ATTN_MMA_SS_X4(NAME, CG)                                                                 \
+#define ATTN_MMA_SS_X4(NAME, CG, KIND)                                                           \
   __device__ __forceinline__ void NAME(uint32_t d, const uint32_t(&alo)[4], uint32_t ahi,       \
                                        const uint32_t(&blo)[4], uint32_t bhi, uint32_t idesc,   \
                                        uint32_t acc) {                                          \
@@ -339,21 +345,22 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "mov.b64 a2, {%3, %9};\n\tmov.b64 a3, {%4, %9};\n\t"                                    \
         "mov.b64 b0, {%5, %10};\n\tmov.b64 b1, {%6, %10};\n\t"                                  \
         "mov.b64 b2, {%7, %10};\n\tmov.b64 b3, {%8, %10};\n\t"                                  \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a0, b0, %11, p;\n\t"                     \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a1, b1, %11, t;\n\t"                     \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a2, b2, %11, t;\n\t"                     \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], a3, b3, %11, t;\n\t}\n" ::"r"(d),        \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], a0, b0, %11, p;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], a1, b1, %11, t;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], a2, b2, %11, t;\n\t"                     \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], a3, b3, %11, t;\n\t}\n" ::"r"(d),        \
         "r"(alo[0]), "r"(alo[1]), "r"(alo[2]), "r"(alo[3]), "r"(blo[0]), "r"(blo[1]),           \
         "r"(blo[2]), "r"(blo[3]), "r"(ahi), "r"(bhi), "r"(idesc), "r"(acc)                      \
         : "memory");                                                                            \
   }
-ATTN_MMA_SS_X4(mma_ss_x4, "1")
-ATTN_MMA_SS_X4(mma_pair_ss_x4, "2")
+ATTN_MMA_SS_X4(mma_ss_x4, "1", "f16")
+ATTN_MMA_SS_X4(mma_pair_ss_x4, "2", "f16")
+ATTN_MMA_SS_X4(mma_ss_x4_f8, "1", "f8f6f4")   // e4m3 operands: 32 per MMA along K
 #undef ATTN_MMA_SS_X4
 
 // Same with A read from tensor memory: A of MMA i starts at column a_tmem + 8 i
 // (sixteen bf16 values of K per MMA, two per 32-bit column).
-#define ATTN_MMA_TS_X4(NAME, CG)                                                                 \
+#define ATTN_MMA_TS_X4(NAME, CG, KIND)                                                           \
   __device__ __forceinline__ void NAME(uint32_t d, uint32_t a_tmem, const uint32_t(&blo)[4],    \
                                        uint32_t bhi, uint32_t idesc, uint32_t acc) {            \
     asm volatile(                                                                               \
@@ -363,16 +370,19 @@ ATTN_MMA_SS_X4(mma_pair_ss_x4, "2")
         "mov.b64 b0, {%2, %6};\n\tmov.b64 b1, {%3, %6};\n\t"                                    \
         "mov.b64 b2, {%4, %6};\n\tmov.b64 b3, {%5, %6};\n\t"                                    \
         "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"                  \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [%1], b0, %8, p;\n\t"                    \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x1], b1, %8, t;\n\t"                    \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x2], b2, %8, t;\n\t"                    \
-        "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),       \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], [%1], b0, %8, p;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], [x1], b1, %8, t;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], [x2], b2, %8, t;\n\t"                    \
+        "@e tcgen05.mma.cta_group::" CG ".kind::" KIND " [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),       \
         "r"(a_tmem), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]), "r"(blo[3]), "r"(bhi), "r"(acc),    \
         "r"(idesc)                                                                              \
         : "memory");                                                                            \
   }
-ATTN_MMA_TS_X4(mma_ts_x4, "1")
-ATTN_MMA_TS_X4(mma_pair_ts_x4, "2")
+ATTN_MMA_TS_X4(mma_ts_x4, "1", "f16")
+ATTN_MMA_TS_X4(mma_pair_ts_x4, "2", "f16")
+// e4m3 A from tensor memory: four values per 32-bit column, so the eight
+// columns per MMA again hold its 32 values of K
+ATTN_MMA_TS_X4(mma_ts_x4_f8, "1", "f8f6f4")
 #undef ATTN_MMA_TS_X4
 
 // Low and high 32-bit halves of the 128-byte-swizzle shared-memory descriptor
@@ -437,6 +447,13 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 }
 
 // ----------------------------------------------------------- small helpers
+// Four floats to e4m3 (round to nearest, saturating), byte i = value i.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  unsigned short lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -446,6 +463,12 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "f"(a), "f"(b),

@@ -69,6 +69,7 @@ cudaError_t launch_tile_lists(const uint8_t* mask, int n, int causal, bool outer
   int* counts = buf + (size_t)nouter * ninner;
   tile_lists_kernel<<<ceil_div(nouter, 128), 128, 0, st>>>(mask, n, causal, outer_is_query ? 1 : 0,
                                                           osz, members, isz, lists, counts, ninner);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -19,8 +19,12 @@ low-precision formats.  Readings taken here:
     2^-9.  Rounding is to the nearest value, ties to the even code (even
     mantissa); magnitudes above 448 saturate to 448.
   * Scaling is per head: descale_h = amax_h / 448 over the head's n x d
-    values, code = round(x / descale_h), and the code stands for
-    code * descale_h.  A head of zeros gets descale 1.
+    values, and the code stands for code * descale_h.  The value rounded is
+    x * (448 / amax_h) formed in float32 (the reciprocal rounded to float32,
+    then the product rounded to float32): where a floating-point value
+    decides an integer code, it is decided in the device's precision, and
+    with bf16 inputs and a bf16 amax exact rounding ties are common.  A head
+    of zeros gets descale 1 and codes 0.
   * Incoherent processing multiplies every row of Q and of K by the same
     orthogonal matrix R = diag(s) H_d / sqrt(d) (H_d the Sylvester Hadamard
     matrix, s a vector of random signs) before quantising.  Since
@@ -80,14 +84,16 @@ def quantize_per_head(x, signs=None):
     rotation of incoherent processing.
 
     Returns (codes, descale, scaled): codes are the e4m3 values (float64),
-    descale has x's leading shape, and scaled = (rotated) x / descale is the
-    value that was rounded (used by tests to recognise rounding ties)."""
+    descale has x's leading shape, and scaled = float32((rotated) x) *
+    float32(448 / amax) is the value that was rounded."""
     x = np.asarray(x, dtype=np.float64)
     if signs is not None:
         x = x @ rotation(x.shape[-1], signs)
     amax = np.abs(x).max(axis=(-2, -1))
     descale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
-    scaled = x / descale[..., None, None]
+    amax32 = np.where(amax > 0, amax, 1.0).astype(np.float32)
+    inv = np.where(amax > 0, np.float32(E4M3_MAX) / amax32, np.float32(1.0)).astype(np.float32)
+    scaled = (x.astype(np.float32) * inv[..., None, None]).astype(np.float64)
     return round_e4m3(scaled), descale, scaled
 
 

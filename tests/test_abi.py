@@ -155,6 +155,42 @@ def test_sparse_argument_checks(L):
                              None) == 1
 
 
+def test_fp8_argument_checks(L):
+    MIS4 = ctypes.c_void_p((1 << 20) + 2)
+
+    def call(d=128, n=256, scale=0.1, dsq=None, q=FAKE, causal=0):
+        return L.attn_fwd_fp8(q, FAKE, FAKE, FAKE, FAKE, 1, 2, n, d, scale, dsq, FAKE, None,
+                              causal, None)
+    assert call(d=64) == 2
+    assert call(n=100) == 2
+    assert call(scale=float("nan")) == 1
+    assert call(causal=3) == 1
+    assert call(dsq=MIS4) == 1
+    assert call(q=MIS) == 1
+    assert call(q=ctypes.c_void_p(0)) == 1
+
+
+def test_quantize_fp8_argument_checks(L):
+    MIS4 = ctypes.c_void_p((1 << 20) + 2)
+    ws = L.attn_quantize_fp8_workspace_size(4, 1000, 128)
+    assert ws == 4 * 8 * 4                              # one float per 128-row block
+    assert L.attn_quantize_fp8_workspace_size(4, 1000, 64) == 0
+
+    def call(n=1024, d=128, tr=0, signs=None, x=FAKE, desc=FAKE, ws_p=FAKE, ws_b=ws):
+        return L.attn_quantize_fp8(x, FAKE, desc, 4, n, d, tr, signs, ws_p, ws_b, None)
+    assert call(d=64) == 2
+    assert call(n=1000, tr=1) == 2                      # transposed rows of n bytes
+    assert call(tr=1, signs=FAKE) == 1                  # V is never rotated
+    assert call(tr=2) == 1
+    assert call(n=0) == 1
+    assert call(x=MIS) == 1
+    assert call(desc=ctypes.c_void_p(0)) == 1
+    assert call(desc=MIS4) == 1
+    assert call(signs=MIS4) == 1
+    assert call(ws_p=ctypes.c_void_p(0)) == 3
+    assert call(ws_b=ws - 1) == 3
+
+
 def test_gemm_argument_checks(L):
     g = L.attn_gemm_bf16
     assert g(FAKE, FAKE, FAKE, 1, 128, 128, 60, 1, 1, 1, 1.0, None) == 2   # K % 8

@@ -80,7 +80,7 @@ def test_rotation_spreads_a_one_hot_row():
 
 def test_quantize_error_bound_and_amax():
     rng = np.random.default_rng(3)
-    x = rng.standard_normal((2, 3, 64, 32))
+    x = rng.standard_normal((2, 3, 64, 32)).astype(np.float32).astype(np.float64)
     x[1, 2] = 0.0                                   # an all-zero head
     codes, descale, scaled = fp8.quantize_per_head(x)
     assert descale[1, 2] == 1.0 and np.all(codes[1, 2] == 0)
@@ -92,8 +92,29 @@ def test_quantize_error_bound_and_amax():
     err = np.abs(codes - scaled)
     bound = np.maximum(2.0 ** -4 * np.abs(scaled), 2.0 ** -10)
     assert np.all(err <= bound * (1 + 1e-12))
+    # scaled is x / descale up to the two float32 roundings of the scaling
+    exact = x / descale[..., None, None]
+    assert np.all(np.abs(scaled - exact) <= 2 * 2.0 ** -24 * np.abs(exact) * (1 + 1e-9))
     deq = fp8.dequantize(codes, descale)
-    assert np.all(np.abs(deq - x) <= bound * descale[..., None, None] * (1 + 1e-12))
+    assert np.all(np.abs(deq - x) <= (bound + 2 * 2.0 ** -24 * np.abs(exact))
+                  * descale[..., None, None] * (1 + 1e-9))
+
+
+def test_quantize_decides_ties_in_float32():
+    # bf16 inputs with amax = 3.5 make 448 / amax = 128 exact: x * 128 lands on
+    # e4m3 midpoints and ties go to the even code
+    x = np.zeros((1, 4, 4))
+    x[0, 0, 0] = 3.5
+    x[0, 1, 0] = 1.0625 / 128        # 1.0625: midpoint of 1 and 1.125 -> 1
+    x[0, 2, 0] = 1.1875 / 128        # midpoint of 1.125 and 1.25 -> 1.25
+    codes, descale, scaled = fp8.quantize_per_head(x)
+    assert descale[0] == 3.5 / 448 and scaled[0, 0, 0] == 448.0
+    assert codes[0, 1, 0] == 1.0 and codes[0, 2, 0] == 1.25
+    # amax = 3.0: 448 / 3 is not exact; the float32 reciprocal decides
+    x[0, 0, 0] = 3.0
+    inv = np.float32(448.0) / np.float32(3.0)
+    codes, _, scaled = fp8.quantize_per_head(x)
+    assert scaled[0, 1, 0] == float(np.float32(1.0625 / 128) * inv)
 
 
 def test_incoherent_processing_shrinks_amax_of_outlier_rows():
