@@ -250,6 +250,51 @@ def traffic_per_launch(w):
     return d.get("dram_bytes_per_launch_full_workload")
 
 
+def e2e_ms_pipelined(step, bufsets, hx, ho, steps, st):
+    """Elapsed ms of `steps` steps through the public API with host buffers:
+    every step copies its inputs from pinned host memory (hx) into one of the
+    device buffer sets, runs step(bufs) on stream st and copies its results
+    (the keys of ho) back to pinned host memory.  Host-to-device and
+    device-to-host copies run on their own streams, so the copies of one step
+    overlap the kernels of its neighbours; events keep each buffer set from
+    being refilled before its step has read it, or reused before its results
+    have been copied out."""
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    nb = len(bufsets)
+    ready = [torch.cuda.Event() for _ in range(nb)]
+    done = [torch.cuda.Event() for _ in range(nb)]
+    drained = [torch.cuda.Event() for _ in range(nb)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(st)
+    cin.wait_event(t0)
+    cout.wait_event(t0)
+    for i in range(steps):
+        j = i % nb
+        bufs = bufsets[j]
+        if i >= nb:
+            cin.wait_event(done[j])          # step i - nb has read these inputs
+        with torch.cuda.stream(cin):
+            for name, h in hx.items():
+                bufs[name].copy_(h, non_blocking=True)
+        ready[j].record(cin)
+        st.wait_event(ready[j])
+        if i >= nb:
+            st.wait_event(drained[j])        # results of step i - nb are out
+        step(bufs)
+        done[j].record(st)
+        cout.wait_event(done[j])
+        with torch.cuda.stream(cout):
+            for name, h in ho.items():
+                h.copy_(bufs[name], non_blocking=True)
+        drained[j].record(cout)
+    st.wait_stream(cout)
+    t1.record(st)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
 def run_ours(args, w):
     from io_aware_exact_05_gb300 import attn
 
@@ -270,6 +315,7 @@ def run_ours(args, w):
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    buf0 = {"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
     wsb = attn.attn_bwd_gqa_workspace_size(w.B, w.H, w.kv_heads, w.n, w.d, attn.ATTN_BF16,
                                            w.causal, mode)
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
@@ -287,7 +333,9 @@ def run_ours(args, w):
                                                                attn.ATTN_BF16, w.causal, mode),
                            dtype=torch.uint8, device=dev)
 
-    def step(e=None):
+    def step(b=buf0, e=None):
+        q, k, v, do, o, lse, dq, dk, dv = (b[n] for n in ("q", "k", "v", "do", "o", "lse",
+                                                           "dq", "dk", "dv"))
         if e: e[0].record(st)
         if bmask is not None:   # the sparse backward is one call: timed as the dK/dV stage
             attn.attn_fwd_sparse(q, k, v, o, lse, sc, w.causal, bmask, fws, st)
@@ -328,7 +376,7 @@ def run_ours(args, w):
     n_launch0 = attn.attn_launch_count()
     t0.record(st)
     for i in range(args.steps):
-        step(ev[i])
+        step(buf0, ev[i])
     t1.record(st)
     launches = attn.attn_launch_count() - n_launch0
     torch.cuda.synchronize()
@@ -353,36 +401,24 @@ def run_ours(args, w):
 
     # ---- end to end through the public API with host buffers
     hx = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
-    ho = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-          for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    ho = {n: torch.empty(buf0[n].shape, dtype=buf0[n].dtype, pin_memory=True)
+          for n in ("o", "lse", "dq", "dk", "dv")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(3, args.steps // 4)
-
-    def e2e_step():
-        for n_, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            dst.copy_(hx[n_], non_blocking=True)
-        step()
-        for n_, src_ in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            ho[n_].copy_(src_, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_steps = max(4, args.steps // 4)
+    buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
+    e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
         tdist.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(st)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(st)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b)
+    e2e_ms = e2e_ms_pipelined(step, [buf0, buf1], hx, ho, e2e_steps, st)
     if dist:
         tt = torch.tensor([e2e_ms], device=dev)
         tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after the end-to-end run: " + attn.attn_strerror(rc))
 
     if rank == 0:
         kv_ms = stage_ms[2]
@@ -418,7 +454,8 @@ def run_ours(args, w):
                          "peak_source": "%s bf16_tflops (burst); sustained %s" % (
                              src, pk.get("bf16_tflops_sustained"))},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "overlap": "two buffer sets; H2D, kernels and D2H on three streams"},
             "gpu_launches": launches,
             "clocks": clk,
         }
@@ -451,20 +488,22 @@ def run_fp8(args, w):
     k8 = torch.empty_like(q8)
     vt8 = torch.empty(w.B, w.H, w.d, w.n, dtype=torch.float8_e4m3fn, device=dev)
     ds = [torch.empty(w.B, w.H, dtype=torch.float32, device=dev) for _ in range(3)]
+    buf0 = {"q": q, "k": k, "v": v, "o": None, "lse": None}
     qws = torch.empty(max(4, attn.attn_quantize_fp8_workspace_size(BH, w.n, w.d)),
                       dtype=torch.uint8, device=dev)
     o = torch.empty(w.B, w.H, w.n, w.d, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)
+    buf0["o"], buf0["lse"] = o, lse
     st = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
 
-    def step(e=None):
+    def step(b=buf0, e=None):
         if e: e[0].record(st)
-        attn.attn_quantize_fp8(q, q8, ds[0], False, None, qws, st)
-        attn.attn_quantize_fp8(k, k8, ds[1], False, None, qws, st)
-        attn.attn_quantize_fp8(v, vt8, ds[2], True, None, qws, st)
+        attn.attn_quantize_fp8(b["q"], q8, ds[0], False, None, qws, st)
+        attn.attn_quantize_fp8(b["k"], k8, ds[1], False, None, qws, st)
+        attn.attn_quantize_fp8(b["v"], vt8, ds[2], True, None, qws, st)
         if e: e[1].record(st)
-        attn.attn_fwd_fp8(q8, k8, vt8, o, lse, w.scale, w.causal, *ds, stream=st)
+        attn.attn_fwd_fp8(q8, k8, vt8, b["o"], b["lse"], w.scale, w.causal, *ds, stream=st)
         if e: e[2].record(st)
 
     for _ in range(args.warmup):
@@ -483,7 +522,7 @@ def run_fp8(args, w):
     n_launch0 = attn.attn_launch_count()
     t0.record(st)
     for i in range(args.steps):
-        step(ev[i])
+        step(buf0, ev[i])
     t1.record(st)
     launches = attn.attn_launch_count() - n_launch0
     torch.cuda.synchronize()
@@ -505,37 +544,24 @@ def run_fp8(args, w):
 
     # ---- end to end: bf16 inputs from pinned host memory, O and LSE back
     hx = {n: x[n].pin_memory() for n in ("q", "k", "v")}
-    dx = {"q": q, "k": k, "v": v}
-    ho = {"o": torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
-          "lse": torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)}
+    ho = {n: torch.empty(buf0[n].shape, dtype=buf0[n].dtype, pin_memory=True)
+          for n in ("o", "lse")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(3, args.steps // 4)
-
-    def e2e_step():
-        for n_, t in hx.items():
-            dx[n_].copy_(t, non_blocking=True)
-        step()
-        ho["o"].copy_(o, non_blocking=True)
-        ho["lse"].copy_(lse, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_steps = max(4, args.steps // 4)
+    buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
+    e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
         tdist.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(st)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(st)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b)
+    e2e_ms = e2e_ms_pipelined(step, [buf0, buf1], hx, ho, e2e_steps, st)
     if dist:
         tt = torch.tensor([e2e_ms], device=dev)
         tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    rc = attn.attn_status()
+    if rc:
+        raise RuntimeError("device status after the end-to-end run: " + attn.attn_strerror(rc))
 
     if rank == 0:
         pk, src = peaks()
@@ -568,7 +594,8 @@ def run_fp8(args, w):
                                   "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
                                   "frac": q_gbs / float(pk["hbm_gbs"])},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "overlap": "two buffer sets; H2D, kernels and D2H on three streams"},
             "gpu_launches": launches,
             "clocks": clk,
         }
