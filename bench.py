@@ -231,7 +231,7 @@ def run_reference(args, w):
 # ------------------------------------------------------------------ our arm
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("bwd_kv128.cu", "sm100.cuh"):
+    for name in ("bwd_kv.cuh", "bwd_kv128.cu", "sm100.cuh"):
         h.update(open(os.path.join(ROOT, "io_aware_exact_05_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 

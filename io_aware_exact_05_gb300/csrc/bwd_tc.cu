@@ -735,7 +735,9 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
                                 gsplit, tl, n, n_pad, scale, causal, ctl, st)
   const bool dq = dQacc != nullptr;
   switch (d) {
-    case 64: if (dq) { ATTN_KV(64, true); } else { ATTN_KV(64, false); }
+    case 64:
+      return launch_bwd_kv64_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit,
+                                tl, n, n_pad, scale, causal, ctl, st);
     case 128:
       return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit,
                                  tl, n, n_pad, scale, causal, ctl, st);

@@ -65,6 +65,13 @@ __device__ __forceinline__ int2 unit_of(int k, const TileRange& tr) {
 __device__ __forceinline__ int pos_of(int t, int j, const TileRange& tr) {
   return min(j, tr.last0 + 1) + min(j, tr.last1 + 1) + ((t == 1 && j <= tr.last0) ? 1 : 0);
 }
+// PV of unit k is followed by S of unit k + 2; when that is the same tile's
+// next step, the S commit covers the PV, which then gets no commit of its own
+// (both sides evaluate this to keep the O-done phases in step).
+__device__ __forceinline__ bool pv_implied(int t, int j, const TileRange& tr) {
+  const int last = t == 0 ? tr.last0 : tr.last1;
+  return j < last && pos_of(t, j + 1, tr) == pos_of(t, j, tr) + 2;
+}
 
 __global__ void __launch_bounds__(384, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -224,7 +231,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int i = 0; i < 4; ++i) blo[i] = v_lo + s * (C::V_BYTES >> 4) + 2 * i;
         mma_ts_x4_f8(tmem + C::O_COL + u.x * D, tmem + C::S_COL + (k & 1) * BN, blo, HI, idesc_o,
                      u.y > 0);
-        tc_commit(bar(F_OD + u.x));
+        if (!pv_implied(u.x, u.y, tr)) tc_commit(bar(F_OD + u.x));
         if (last_user(u.x, u.y)) tc_commit(bar(F_VE + s));
         if (k + 2 < total) ok = issue_s(k + 2);
       }
@@ -248,6 +255,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int last = (t == 0) ? tr.last0 : tr.last1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float m = -INFINITY, l = 0.f;
+    int odc = 0;   // O-done phases consumed
     bool ok = true;
     for (int j = 0; j <= last; ++j) {
       const int k = pos_of(t, j, tr);
@@ -304,9 +312,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const float rs = rs2.x + rs2.y;
       tmem_st_wait();
       l = l * alpha + rs;
-      if (j > 0) {   // PV of tile j-1 done (waited every iteration: parity stays unambiguous)
-        ok = mbar_wait_warp(bar(F_OD + t), (j - 1) & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+      if (j > 0 && !pv_implied(t, j - 1, tr)) {   // PV of step j-1 done before any rescale
+        ok = mbar_wait_warp(bar(F_OD + t), odc & 1, abort_flag, ctl, SITE_FWD_O_DONE);
         if (!ok) break;
+        ++odc;
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // kept maximum moved
         tc_fence_after();
@@ -333,7 +342,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       mbar_arrive(bar(F_PF + slot));
     }
     if (ok && last >= 0) {
-      ok = mbar_wait_warp(bar(F_OD + t), last & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+      ok = mbar_wait_warp(bar(F_OD + t), odc & 1, abort_flag, ctl, SITE_FWD_O_DONE);   // last PV
       if (ok) {
         tc_fence_after();
         const float mul = descale_v / l;

@@ -79,6 +79,15 @@ __device__ __forceinline__ Unit unit_at(int k, const TileInfo& ti) {
 __device__ __forceinline__ int unit_pos(int t, int j, const TileInfo& ti) {
   return min(j, ti.last0 + 1) + min(j, ti.last1 + 1) + ((t == 1 && j <= ti.last0) ? 1 : 0);
 }
+// The issuer follows PV of unit k with S of unit k + 2.  When that S is the
+// same query tile's next KV step, the commit that tells the tile's softmax
+// "S ready" also covers the PV before it (a commit tracks every earlier MMA
+// of its thread), so that PV needs no commit of its own and the softmax no
+// wait for it.  Both sides evaluate this to keep the O-done phases in step.
+__device__ __forceinline__ bool pv_implied(int t, int j, const TileInfo& ti) {
+  const int last = t == 0 ? ti.last0 : ti.last1;
+  return j < last && unit_pos(t, j + 1, ti) == unit_pos(t, j, ti) + 2;
+}
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, float mul) {
   uint32_t pk[16];
@@ -278,7 +287,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           for (int i = 0; i < 4; ++i) blo[i] = vb + (4 * b + i) * (2048 / 16);
           mma_ts_x4(tmem + C::O_COL + u.t * D, pa + 32 * b, blo, HI, idesc_o, (u.j > 0 || b > 0));
         }
-        tc_commit(bar(B_OD + u.t));
+        if (!pv_implied(u.t, u.j, ti)) tc_commit(bar(B_OD + u.t));
         if (last_user(u.t, u.j)) tc_commit(bar(B_VE + s));
         if (k + 2 < total) ok = issue_s(k + 2);
       }
@@ -299,6 +308,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int last = (t == 0) ? ti.last0 : ti.last1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float m = -INFINITY, l = 0.f;
+    int odc = 0;   // O-done phases consumed (PVs with a commit of their own)
     bool ok = true;
     for (int j = 0; j <= last; ++j) {
       const int k = unit_pos(t, j, ti);
@@ -362,12 +372,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const float rs = rs2.x + rs2.y;
       tmem_st_wait();
       l = l * alpha + rs;
-      // Wait for PV of tile j-1 every iteration: a parity wait is only
-      // unambiguous while the waiter is at most one phase behind.
-      if (j > 0) {
-        ok = mbar_wait(bar(B_OD + t), (j - 1) & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+      // PV of step j-1 must be done before O is rescaled.  It is when its
+      // completion was implied by the S wait above; otherwise wait for its
+      // own commit (every committed phase is waited for, so a parity wait
+      // is never more than one phase behind).
+      if (j > 0 && !pv_implied(t, j - 1, ti)) {
+        ok = mbar_wait(bar(B_OD + t), odc & 1, abort_flag, ctl, SITE_FWD_O_DONE);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        ++odc;
       }
       // Rescale this row of O when its kept maximum moved.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
@@ -395,7 +408,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_arrive(bar(B_PF + slot));
     }
     if (ok && last >= 0) {
-      ok = mbar_wait(bar(B_OD + t), last & 1, abort_flag, ctl, SITE_FWD_O_DONE);
+      ok = mbar_wait(bar(B_OD + t), odc & 1, abort_flag, ctl, SITE_FWD_O_DONE);   // last PV: committed
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();

@@ -92,8 +92,13 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
 // Tiling of the key-tile kernel for head dim d (key tiles of kv_rows keys,
 // query tiles of query_rows).
 void bwd_kv_tiling(int d, int* kv_rows, int* query_rows);
-// Key-tile backward for d = 128, pipelined two query tiles deep (dQ shares
-// reduced into dQacc with TMA bulk reduce-add when dQacc != nullptr).
+// Key-tile backward for d = 64 and d = 128, pipelined two query tiles deep
+// (dQ shares reduced into dQacc with TMA bulk reduce-add when dQacc != nullptr).
+int launch_bwd_kv64_tc(const void* Q, const void* K, const void* V, const void* dO,
+                       const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                       float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
+                       const TileLists& tl, int n, int n_pad, float scale, int causal,
+                       const KernelCtl& ctl, cudaStream_t st);
 int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void* dO,
                         const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
                         float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
