@@ -250,6 +250,22 @@ def traffic_per_launch(w):
     return d.get("dram_bytes_per_launch_full_workload")
 
 
+def preprocess_roofline(w, mode_used, ms, pk, src):
+    """HBM roofline of the D preprocess (delta_kernel): it reads O, dO and LSE,
+    writes D and LSE2 (rows padded to 128) and, in atomic dQ mode, zeroes the
+    fp32 dQ accumulator."""
+    rows = w.B * w.H * w.n
+    rows_pad = w.B * w.H * ((w.n + 127) // 128 * 128)
+    nbytes = 2 * rows * w.d * 2 + rows * 4 + 2 * rows_pad * 4
+    if mode_used == "atomic":
+        nbytes += rows * w.d * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = float(pk["hbm_gbs"])
+    return {"kernel": "delta_kernel (attn_bwd_preprocess)", "bound": "hbm",
+            "bytes_per_launch": nbytes, "achieved": gbs, "peak": peak, "unit": "GB/s",
+            "frac": gbs / peak, "peak_source": "%s hbm_gbs" % src}
+
+
 def e2e_ms_pipelined(step, bufsets, hx, ho, steps, st):
     """Elapsed ms of `steps` steps through the public API with host buffers:
     every step copies its inputs from pinned host memory (hx) into one of the
@@ -446,6 +462,8 @@ def run_ours(args, w):
                          "bwd_dkdv": stage_ms[2], "bwd_dq": stage_ms[3]},
             "tflops": {"fwd": fl["fwd"] / (stage_ms[0] * 1e-3) / 1e12,
                        "bwd": fl["bwd"] / (sum(stage_ms[1:]) * 1e-3) / 1e12},
+            "preprocess": preprocess_roofline(w, mode_used, stage_ms[1], pk, src)
+                          if not (grouped or bmask is not None) else None,
             "roofline": {"kernel": "%s (attn_bwd_dkdv)" % (
                              "bwd_kv128_kernel" if w.d == 128 else "bwd_kv_kernel"),
                          "bound": "tensor", "flops_per_launch": kv_flops,

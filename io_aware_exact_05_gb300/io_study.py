@@ -24,15 +24,23 @@ Run one path and configuration per process under ncu, then summarise:
     python -m io_aware_exact_05_gb300.io_study summarize io_*.csv
 
 `run` does one forward and one backward of the path on B=1, H=4 synthetic
-heads, non-causal.  `summarize` sums the backward launches of each file
+heads, non-causal (--B, --H, --causal change that).  `summarize` sums the backward launches of each file
 (fused: every launch after the forward kernel; materialise-P: every launch
 after its three forward launches) and prints bytes per path with reference
 counts: the compulsory bytes and n^2 d^2 / M with M the K, V tile a CTA keeps
 on chip.
+
+`kernels` reads a launch list taken with
+`ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum`
+and prints, per launch, its time, DRAM bytes and DRAM GB/s against the
+measured HBM copy bandwidth (the bound of the HBM-bound kernels: the D
+preprocess, the dQ conversion and the materialise-P row kernels).
 """
 
 import argparse
 import csv
+import json
+import os
 import re
 import sys
 
@@ -41,26 +49,26 @@ __all__ = ["main"]
 B, H = 1, 4
 
 
-def _run(path, n, d):
+def _run(path, n, d, b=B, h=H, causal=False):
     import torch
 
     from . import attn
     from .inputs import Workload, make_inputs
 
-    w = Workload("io", B, H, n, d, "bf16", False, 1.0, 2000 + n + d)
+    w = Workload("io", b, h, n, d, "bf16", causal, 1.0, 2000 + n + d)
     x = make_inputs(w)
     dev = torch.device("cuda", 0)
     q, k, v, do = (x[t].to(dev) for t in ("q", "k", "v", "do"))
     if path == "fused":   # tiled forward, then the tiled backward (key-tile kernel + dQ)
-        o, lse = attn.forward(q, k, v)
-        attn.backward(q, k, v, o, do, lse)
+        o, lse = attn.forward(q, k, v, causal=causal)
+        attn.backward(q, k, v, o, do, lse, causal=causal)
     else:                 # materialise-P: S, P, dP, dS as n x n matrices in HBM
-        ws = torch.empty(attn.attn_mat_workspace_size(B, H, n, d), dtype=torch.uint8,
+        ws = torch.empty(attn.attn_mat_workspace_size(b, h, n, d), dtype=torch.uint8,
                          device=dev)
-        o, lse = torch.empty_like(q), torch.empty(B, H, n, device=dev)
-        attn.attn_mat_fwd(q, k, v, o, lse, w.scale, False, ws)
+        o, lse = torch.empty_like(q), torch.empty(b, h, n, device=dev)
+        attn.attn_mat_fwd(q, k, v, o, lse, w.scale, causal, ws)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        attn.attn_mat_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, False, ws)
+        attn.attn_mat_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, causal, ws)
     torch.cuda.synchronize()
     rc = attn.attn_status()
     if rc:
@@ -74,7 +82,8 @@ def _rows(path):
     ki, mi, ui, vi = (h.index("Kernel Name"), h.index("Metric Name"), h.index("Metric Unit"),
                       h.index("Metric Value"))
     idi = h.index("ID")
-    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9,   # bytes
+             "ns": 1, "nsecond": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}   # ns
     launches = {}
     for r in rows[hi + 1:]:
         if len(r) <= vi:
@@ -129,6 +138,28 @@ def _summarize(paths):
             r["fused_l2"] / r["n2d2_over_m"]))
 
 
+def _hbm_peak():
+    p = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                     "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernels(path):
+    peak, src = _hbm_peak()
+    print("| # | kernel | time us | DRAM MB (read + write) | DRAM GB/s | of %s %.0f GB/s |"
+          % (src, peak))
+    print("|---|---|---|---|---|---|")
+    for i, l in enumerate(_rows(path)):
+        t = l.get("gpu__time_duration.sum", 0.0)   # ns
+        rd = l.get("dram__bytes_read.sum", 0.0)
+        wr = l.get("dram__bytes_write.sum", 0.0)
+        gbs = (rd + wr) / t if t > 0 else 0.0        # bytes / ns = GB/s
+        print("| %d | %s | %.1f | %.1f + %.1f | %.0f | %.1f %% |" % (
+            i, l["name"], t / 1e3, rd / 1e6, wr / 1e6, gbs, 100.0 * gbs / peak))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     sub = ap.add_subparsers(dest="cmd", required=True)
@@ -136,11 +167,18 @@ def main(argv=None):
     r.add_argument("--path", choices=["fused", "mat"], required=True)
     r.add_argument("--n", type=int, required=True)
     r.add_argument("--d", type=int, required=True)
+    r.add_argument("--B", type=int, default=B)
+    r.add_argument("--H", type=int, default=H)
+    r.add_argument("--causal", action="store_true")
     s = sub.add_parser("summarize")
     s.add_argument("csv", nargs="+")
+    kk = sub.add_parser("kernels")
+    kk.add_argument("csv")
     a = ap.parse_args(argv)
     if a.cmd == "run":
-        _run(a.path, a.n, a.d)
+        _run(a.path, a.n, a.d, a.B, a.H, a.causal)
+    elif a.cmd == "kernels":
+        _kernels(a.csv)
     else:
         _summarize(a.csv)
 
