@@ -59,6 +59,29 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload(w, rank):
+    """Each rank draws its own batch: the same shapes, the seed offset by the
+    rank (weak scaling: every rank processes a full workload)."""
+    return w.with_shape(seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (the job's elapsed time is its
+    slowest rank's); x itself without a process group."""
+    if not dist:
+        return x
+    import torch.distributed as tdist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step, world, steps, ms):
+    """Whole-job throughput: the FLOPs every rank did over the slowest rank's time."""
+    return flops_per_step * world * steps / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -325,7 +348,7 @@ def run_ours(args, w):
     mode = {"atomic": attn.ATTN_DQ_ATOMIC, "pass": attn.ATTN_DQ_PASS,
             "auto": attn.ATTN_DQ_AUTO}[args.mode]
     mode_used = args.mode if args.mode != "auto" else ("atomic" if w.d <= 128 else "pass")
-    wr = w.with_shape(seed=w.seed + 7919 * rank)    # each rank its own batch
+    wr = rank_workload(w, rank)
     x = make_inputs(wr)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
@@ -400,10 +423,7 @@ def run_ours(args, w):
         tdist.barrier()
     clk = clocks.stop()
     el_ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([el_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        el_ms = float(tt.item())
+    el_ms = max_over_ranks(el_ms, dist, dev)
     rc = attn.attn_status()
     if rc:
         raise RuntimeError("device status after timing: " + attn.attn_strerror(rc))
@@ -412,7 +432,7 @@ def run_ours(args, w):
 
     fl = step_flops(w)
     per_step = fl["total"]
-    value = per_step * ws_n * args.steps / (el_ms * 1e-3) / 1e12
+    value = whole_job_tflops(per_step, ws_n, args.steps, el_ms)
     pk, src = peaks()
 
     # ---- end to end through the public API with host buffers
@@ -427,11 +447,8 @@ def run_ours(args, w):
     if dist:
         tdist.barrier()
     e2e_ms = e2e_ms_pipelined(step, [buf0, buf1], hx, ho, e2e_steps, st)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_val = whole_job_tflops(per_step, ws_n, e2e_steps, e2e_ms)
     rc = attn.attn_status()
     if rc:
         raise RuntimeError("device status after the end-to-end run: " + attn.attn_strerror(rc))
@@ -498,7 +515,7 @@ def run_fp8(args, w):
         tdist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wr = w.with_shape(seed=w.seed + 7919 * rank)    # each rank its own batch
+    wr = rank_workload(w, rank)
     x = make_inputs(wr)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     BH = w.B * w.H
@@ -548,17 +565,14 @@ def run_fp8(args, w):
         tdist.barrier()
     clk = clocks.stop()
     el_ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([el_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        el_ms = float(tt.item())
+    el_ms = max_over_ranks(el_ms, dist, dev)
     rc = attn.attn_status()
     if rc:
         raise RuntimeError("device status after timing: " + attn.attn_strerror(rc))
     stage_ms = [sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(args.steps)) / args.steps
                 for s in range(2)]
     per_step = step_flops(w)["total"]
-    value = per_step * ws_n * args.steps / (el_ms * 1e-3) / 1e12
+    value = whole_job_tflops(per_step, ws_n, args.steps, el_ms)
 
     # ---- end to end: bf16 inputs from pinned host memory, O and LSE back
     hx = {n: x[n].pin_memory() for n in ("q", "k", "v")}
@@ -572,11 +586,8 @@ def run_fp8(args, w):
     if dist:
         tdist.barrier()
     e2e_ms = e2e_ms_pipelined(step, [buf0, buf1], hx, ho, e2e_steps, st)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_val = per_step * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_val = whole_job_tflops(per_step, ws_n, e2e_steps, e2e_ms)
     rc = attn.attn_status()
     if rc:
         raise RuntimeError("device status after the end-to-end run: " + attn.attn_strerror(rc))
