@@ -329,6 +329,18 @@ ATTN_API int attn_gemm_bf16(const void* A, const void* Bm, void* C, int batch, i
  * error recorded since the last call (ATTN_OK if none). */
 ATTN_API int attn_status(void* stream);
 
+/*
+ * attn_selftest_wait_timeout -- checks that device-side failure detection
+ * reaches the host.  Every barrier wait inside the library's kernels is
+ * bounded: when it runs out it records ATTN_ERR_DEVICE_TIMEOUT (and the wait
+ * site) in the device status word and the kernel returns instead of hanging.
+ * This launches one block whose single wait has no arrival, with the limit
+ * timeout_ns (1 us .. 10 s; ATTN_ERR_INVALID_ARG otherwise): after it, the
+ * next attn_status(stream) returns ATTN_ERR_DEVICE_TIMEOUT and the context
+ * stays usable.  No fault is involved.
+ */
+ATTN_API int attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
 /* Number of kernels the library has enqueued in this process so far
  * (every launch by every entry point, counted on the host when it is
  * issued).  The difference across a region is how many of the library's

@@ -23,10 +23,13 @@ __all__ = [
     "attn_bwd_sparse_workspace_size",
     "attn_mat_fwd", "attn_mat_bwd", "attn_mat_workspace_size",
     "attn_gemm_bf16", "attn_status", "attn_strerror", "attn_version", "attn_launch_count",
+    "attn_selftest_wait_timeout",
     "forward", "backward",
 ]
 
 ATTN_BF16, ATTN_F32 = 0, 1
+(ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA,
+ ATTN_ERR_DEVICE_TIMEOUT) = range(6)
 ATTN_DQ_AUTO, ATTN_DQ_ATOMIC, ATTN_DQ_PASS = 0, 1, 2
 
 _LIB = None
@@ -101,6 +104,8 @@ def lib():
             L.attn_strerror.argtypes = [i]
             L.attn_strerror.restype = ctypes.c_char_p
             L.attn_version.argtypes = []
+            L.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+            L.attn_selftest_wait_timeout.restype = i
             L.attn_launch_count.argtypes = []
             L.attn_launch_count.restype = ctypes.c_ulonglong
             L.attn_version.restype = ctypes.c_char_p
@@ -148,6 +153,13 @@ def attn_version():
 def attn_status(stream=None):
     """Synchronise the stream; return and clear the first device-side error."""
     return lib().attn_status(_stream(stream))
+
+
+def attn_selftest_wait_timeout(timeout_ns, stream=None):
+    """Launch the bounded-wait self-test: one wait with no arrival runs out
+    after timeout_ns, so the next attn_status() returns ATTN_ERR_DEVICE_TIMEOUT."""
+    _check(lib().attn_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
+           "attn_selftest_wait_timeout")
 
 
 def attn_launch_count():

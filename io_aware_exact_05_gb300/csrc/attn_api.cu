@@ -563,6 +563,11 @@ const char* attn_strerror(int code) {
 
 unsigned long long attn_launch_count(void) { return attn::launch_count(); }
 
+int attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  return cuda_rc(launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
 const char* attn_version(void) { return "libattn 0.1 (sm_103a)"; }
 
 }  // extern "C"

@@ -57,6 +57,7 @@ enum WaitSite : int {
   SITE_GEMM_FULL = 301,
   SITE_GEMM_EMPTY = 302,
   SITE_GEMM_ACC = 303,
+  SITE_SELFTEST = 901,
 };
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

@@ -26,6 +26,10 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
 
 KernelCtl default_ctl();
 
+// One block whose only wait has no arrival: records ATTN_ERR_DEVICE_TIMEOUT
+// after timeout_ns and returns (attn_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
+
 // Counts one kernel launch of the library (host side; attn_launch_count).
 void note_launch();
 unsigned long long launch_count();

@@ -191,6 +191,11 @@ def test_quantize_fp8_argument_checks(L):
     assert call(ws_b=ws - 1) == 3
 
 
+def test_selftest_argument_checks(L):
+    assert L.attn_selftest_wait_timeout(0, None) == 1          # below 1 us
+    assert L.attn_selftest_wait_timeout(10**11, None) == 1     # above 10 s
+
+
 def test_gemm_argument_checks(L):
     g = L.attn_gemm_bf16
     assert g(FAKE, FAKE, FAKE, 1, 128, 128, 60, 1, 1, 1, 1.0, None) == 2   # K % 8
