@@ -49,13 +49,39 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
     reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
+// Copies a 128-row bf16 tile held in shared memory as D/64 128-byte-swizzled
+// boxes of [128 rows][64 columns] into tensor memory as an MMA A operand
+// (lane = row, two consecutive elements per 32-bit column, D/2 columns from
+// `tcol`).  Run by one warpgroup: thread r copies row r.
+template <int D>
+__device__ __forceinline__ void tile_to_tmem(const uint8_t* tile, uint32_t tcol, int r) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) {
+    const uint8_t* box = tile + kb * (128 * 128);
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(r, c));
+      w[4 * c] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+    tmem_st32(tcol + 32 * kb, w);
+  }
+  tmem_st_wait();
+}
+
 // ============================================================================ key-tile kernel
 template <int D, bool DQ>
 struct KvCfg {
   static constexpr int BNK = 128;                    // keys per CTA (TMEM lanes)
   static constexpr int BM = (D == 256) ? 64 : 128;   // queries per iteration
   static constexpr int DO = (D == 256) ? 128 : D;    // dK/dV columns per CTA
-  static constexpr int STG = (D == 256) ? 1 : 2;
+  static constexpr int STG = 2;
+  // d = 256: K (the A operand of S^T = K Q^T, constant for the CTA) lives in
+  // tensor memory, which frees the shared memory of a second Q/dO stage
+  static constexpr bool K_IN_TMEM = (D == 256);
   static constexpr bool WITH_DQ = DQ;                // atomic dQ shares from this kernel
   static constexpr bool DS_ALIAS = DQ && D == 128;   // dS reuses the dO stage buffer
   static constexpr int NKB = D / 64;
@@ -63,9 +89,11 @@ struct KvCfg {
   static constexpr uint32_t QT_BYTES = BM * D * 2;   // one Q or dO tile
   static constexpr uint32_t STAT_BYTES = BM * 4;     // LSE2 or D of the tile
   static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024;   // Q, dO, LSE2 + D (padded)
-  static constexpr uint32_t K_OFF = 0;
-  static constexpr uint32_t V_OFF = KV_BYTES;
-  static constexpr uint32_t ST_OFF = 2 * KV_BYTES;
+  static constexpr uint32_t K_OFF = 0;                              // unused when K_IN_TMEM
+  static constexpr uint32_t V_OFF = K_IN_TMEM ? 0 : KV_BYTES;
+  static constexpr uint32_t ST_OFF = K_IN_TMEM ? KV_BYTES : 2 * KV_BYTES;
+  // where K's load lands: the second stage, before that stage's first use
+  static constexpr uint32_t K_LOAD_OFF = K_IN_TMEM ? ST_OFF + STAGE : K_OFF;
   static constexpr uint32_t DS_OFF = ST_OFF + STG * STAGE;  // dedicated dS buffer (D = 64)
   static constexpr uint32_t DS_BYTES = (WITH_DQ && !DS_ALIAS) ? BM * BNK * 2 : 0;
   static constexpr uint32_t BAR_OFF = DS_OFF + DS_BYTES;
@@ -75,15 +103,17 @@ struct KvCfg {
   static constexpr int DK_COL = DO;
   static constexpr int S_COL = 2 * DO;
   static constexpr int DP_COL = 2 * DO + BM;
+  static constexpr int K_COL = 2 * DO + 2 * BM;       // K as A operand (K_IN_TMEM)
   static constexpr int NTHREADS = WITH_DQ ? 512 : 384;
-  static_assert(2 * DO + 2 * BM <= 512, "tensor memory budget");
+  static_assert(2 * DO + 2 * BM + (K_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
+  static_assert(!K_IN_TMEM || (KV_BYTES <= STAGE && !DQ), "K in tensor memory: no dQ here");
   static_assert(!WITH_DQ || (BM == 128 && D <= BM), "dQ tile reuses the S columns");
   static_assert(!(D == 256 && DQ), "d = 256 takes dQ from the query-tile kernel");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8, K_DVD = 9,
-             K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13 };
+             K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13, K_CP = 14 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
 // one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
@@ -142,6 +172,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(K_DQE), 128);
     mbar_init(bar(K_ACC), 1);
     mbar_init(bar(K_DRAIN), 1);
+    mbar_init(bar(K_CP), 128);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -161,7 +192,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_expect_tx(bar(K_KV), 2 * C::KV_BYTES);
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
-        tma_load_3d(sb + C::K_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
+        tma_load_3d(sb + C::K_LOAD_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
         tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
       }
       int issued_last[2] = {-1, -1};
@@ -172,6 +203,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const int s = u % C::STG;
           const int q0 = qtile(ut) * C::BM;
           if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+            go = false;
+            break;
+          }
+          // the second stage holds K until it has been copied to tensor memory
+          if (C::K_IN_TMEM && u == 1 &&
+              !mbar_wait(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV)) {
             go = false;
             break;
           }
@@ -202,6 +239,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS MN-major, K MN-major
       bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      if (C::K_IN_TMEM) ok = ok && mbar_wait_warp(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV);
       const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
       for (int u = 0; ok && u < total; ++u) {
         const int s = u % C::STG;
@@ -217,8 +255,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::S_COL, sdesc_sw128(ka + koff, 16, 1024), sdesc_sw128(qa + qoff, 16, 1024),
-                 id_s, kk > 0);
+          if (C::K_IN_TMEM)   // A = K from tensor memory, 16 elements = 8 columns per MMA
+            mma_ts(tmem + C::S_COL, tmem + C::K_COL + 8 * kk, sdesc_sw128(qa + qoff, 16, 1024),
+                   id_s, kk > 0);
+          else
+            mma_ss(tmem + C::S_COL, sdesc_sw128(ka + koff, 16, 1024),
+                   sdesc_sw128(qa + qoff, 16, 1024), id_s, kk > 0);
         }
         tc_commit(bar(K_SF));
 #pragma unroll
@@ -280,6 +322,16 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
+    if (C::K_IN_TMEM && h == 0) {   // first warpgroup: K rows into tensor memory
+      ok = mbar_wait(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
+      if (__all_sync(0xffffffffu, ok)) {
+        tile_to_tmem<D>(smem + C::K_LOAD_OFF, tmem + lane_off + C::K_COL, r);
+        tc_fence_before();
+        mbar_arrive(bar(K_CP));
+      } else {
+        ok = false;
+      }
+    }
     for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
       for (int ut = 0; ut < cnt; ++ut, ++u) {
         const int s = u % C::STG;
@@ -445,24 +497,32 @@ template <int D>
 struct QCfg {
   static constexpr int BM = 128;                     // queries per CTA (TMEM lanes)
   static constexpr int BN = (D == 256) ? 64 : 128;   // keys per iteration
-  static constexpr int STG = (D == 256) ? 1 : 2;
+  static constexpr int STG = 2;
+  // d = 256: Q (the A operand of S = Q K^T, constant for the CTA) lives in
+  // tensor memory, which frees the shared memory of a second K/V stage
+  static constexpr bool Q_IN_TMEM = (D == 256);
   static constexpr int NKB = D / 64;
   static constexpr uint32_t QT_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t G_OFF = QT_BYTES;
-  static constexpr uint32_t ST_OFF = 2 * QT_BYTES;   // stages of (K_j, V_j)
+  static constexpr uint32_t Q_OFF = 0;                              // unused when Q_IN_TMEM
+  static constexpr uint32_t G_OFF = Q_IN_TMEM ? 0 : QT_BYTES;
+  static constexpr uint32_t ST_OFF = Q_IN_TMEM ? QT_BYTES : 2 * QT_BYTES;   // (K_j, V_j) stages
+  // where Q's load lands: the second stage, before that stage's first use
+  static constexpr uint32_t Q_LOAD_OFF = Q_IN_TMEM ? ST_OFF + 2 * KV_BYTES : Q_OFF;
   static constexpr uint32_t BAR_OFF = ST_OFF + STG * 2 * KV_BYTES;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
   static constexpr int S_COL = 0;
   static constexpr int DP_COL = BN;
   static constexpr int DQ_COL = 2 * BN;
+  static constexpr int Q_COL = 2 * BN + D;            // Q as A operand (Q_IN_TMEM)
   static constexpr int NTHREADS = 384;
-  static_assert(2 * BN + D <= 512, "tensor memory budget");
+  static_assert(2 * BN + D + (Q_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
+  static_assert(!Q_IN_TMEM || QT_BYTES <= 2 * KV_BYTES, "Q fits in the second stage");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum : int { Q_QF = 0, Q_KF = 1, Q_KE = 3, Q_SF = 5, Q_DPF = 6, Q_DSR = 7, Q_ACC = 8, Q_DRAIN = 9 };
+enum : int { Q_QF = 0, Q_KF = 1, Q_KE = 3, Q_SF = 5, Q_DPF = 6, Q_DSR = 7, Q_ACC = 8, Q_DRAIN = 9,
+             Q_CP = 10 };
 
 template <int D>
 __global__ void __launch_bounds__(QCfg<D>::NTHREADS, 1)
@@ -504,6 +564,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     mbar_init(bar(Q_DSR), 256);
     mbar_init(bar(Q_ACC), 1);
     mbar_init(bar(Q_DRAIN), 1);
+    mbar_init(bar(Q_CP), 128);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -522,13 +583,16 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       mbar_expect_tx(bar(Q_QF), 2 * C::QT_BYTES);
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
-        tma_load_3d(sb + C::Q_OFF + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(Q_QF));
+        tma_load_3d(sb + C::Q_LOAD_OFF + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(Q_QF));
         tma_load_3d(sb + C::G_OFF + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(Q_QF));
       }
       int issued_last[2] = {-1, -1};
       for (int j = 0; j < cnt; ++j) {
         const int s = j % C::STG;
         if (!mbar_wait(bar(Q_KE + s), ((j / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+          break;
+        // the second stage holds Q until it has been copied to tensor memory
+        if (C::Q_IN_TMEM && j == 1 && !mbar_wait(bar(Q_CP), 0, abort_flag, ctl, SITE_BWD_Q_FULL))
           break;
         const uint32_t st = sb + C::ST_OFF + s * 2 * C::KV_BYTES;
         mbar_expect_tx(bar(Q_KF + s), 2 * C::KV_BYTES);
@@ -552,6 +616,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);
       constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait_warp(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
+      if (C::Q_IN_TMEM) ok = ok && mbar_wait_warp(bar(Q_CP), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
       const uint32_t qa = sb + C::Q_OFF, ga = sb + C::G_OFF;
       for (int j = 0; ok && j < cnt; ++j) {
         const int s = j % C::STG;
@@ -562,8 +627,12 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::S_COL, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
-                 id_s, kk > 0);
+          if (C::Q_IN_TMEM)   // A = Q from tensor memory, 16 elements = 8 columns per MMA
+            mma_ts(tmem + C::S_COL, tmem + C::Q_COL + 8 * kk, sdesc_sw128(ka + koff, 16, 1024),
+                   id_s, kk > 0);
+          else
+            mma_ss(tmem + C::S_COL, sdesc_sw128(qa + qoff, 16, 1024),
+                   sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
         }
         tc_commit(bar(Q_SF));
 #pragma unroll
@@ -604,6 +673,16 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     const float lse2 = LSE2[(size_t)bh * n_pad + qrow];   // +inf on padded rows -> P = 0
     const float dd = Dv[(size_t)bh * n_pad + qrow];
     bool ok = true;
+    if (C::Q_IN_TMEM && h == 0) {   // first warpgroup: Q rows into tensor memory
+      ok = mbar_wait(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
+      if (__all_sync(0xffffffffu, ok)) {
+        tile_to_tmem<D>(smem + C::Q_LOAD_OFF, tmem + lane_off + C::Q_COL, r);
+        tc_fence_before();
+        mbar_arrive(bar(Q_CP));
+      } else {
+        ok = false;
+      }
+    }
     for (int j = 0; j < cnt; ++j) {
       const int k0 = ktile(j) * C::BN;
       ok = mbar_wait(bar(Q_SF), j & 1, abort_flag, ctl, SITE_BWD_S_FULL);
