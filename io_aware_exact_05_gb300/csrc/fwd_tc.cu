@@ -51,14 +51,18 @@ struct FwdCfg {
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
   static constexpr int S_COL = 0;               // two S slots of BN columns
   static constexpr int O_COL = 2 * BN;          // QT accumulators of D columns
+  // d = 256 (one query tile): Q is the A operand of S = Q K^T from tensor
+  // memory, so the S products read only K from shared memory
+  static constexpr bool Q_IN_TMEM = (D == 256 && QT == 1);
+  static constexpr int Q_COL = 2 * BN + QT * D;
   static constexpr int NTHREADS = 128 * (1 + QT);
-  static_assert(2 * BN + QT * D <= 512, "tensor memory budget");
+  static_assert(2 * BN + QT * D + (Q_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 // Barrier indices inside the barrier block.
 enum : int { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17,
-             B_DRAIN = 19, B_COUNT = 20 };
+             B_DRAIN = 19, B_QC = 20, B_COUNT = 21 };   // B_QC: Q copied to tensor memory
 
 struct TileInfo {
   int last0, last1;   // last KV tile index each query tile needs (-1: none)
@@ -161,6 +165,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar(B_OD + s), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_QC), 128);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -244,6 +249,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       auto first_user = [&](int t, int j) { return t == 0 || j > ti.last0; };
       auto last_user = [&](int t, int j) { return QT == 1 || t == 1 || j > ti.last1; };
       bool ok = mbar_wait_warp(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      if (C::Q_IN_TMEM) ok = ok && mbar_wait_warp(bar(B_QC), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
       // S(k) = Q_t K_j^T into S slot k & 1
       auto issue_s = [&](int k) -> bool {
         const Unit u = unit_at<QT>(k, ti);
@@ -262,7 +268,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             alo[i] = qb + b * (C::BM * 128 / 16) + 2 * i;
             blo[i] = kb + b * (BN * 128 / 16) + 2 * i;
           }
-          mma_ss_x4(tmem + C::S_COL + (k & 1) * BN, alo, HI, blo, HI, idesc_s, b > 0);
+          if (C::Q_IN_TMEM)   // A = Q from tensor memory: box b at columns 32b
+            mma_ts_x4(tmem + C::S_COL + (k & 1) * BN, tmem + C::Q_COL + 32 * b, blo, HI, idesc_s,
+                      b > 0);
+          else
+            mma_ss_x4(tmem + C::S_COL + (k & 1) * BN, alo, HI, blo, HI, idesc_s, b > 0);
         }
         tc_commit(bar(B_SF + (k & 1)));
         if (last_user(u.t, u.j)) tc_commit(bar(B_KE + s));
@@ -310,7 +320,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     float m = -INFINITY, l = 0.f;
     int odc = 0;   // O-done phases consumed (PVs with a commit of their own)
     bool ok = true;
-    for (int j = 0; j <= last; ++j) {
+    if (C::Q_IN_TMEM) {   // the (only) softmax warpgroup copies the Q rows into tensor memory
+      ok = mbar_wait(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tile_to_tmem<D>(smem + C::Q_OFF, tmem + lane_off + C::Q_COL, r);
+        tc_fence_before();
+        mbar_arrive(bar(B_QC));
+      }
+    }
+    for (int j = 0; ok && j <= last; ++j) {
       const int k = unit_pos(t, j, ti);
       const int slot = k & 1;
       const int ent = SPARSE ? slist[j] : j;   // read before the wait hides its latency

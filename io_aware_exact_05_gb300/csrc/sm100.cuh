@@ -482,5 +482,28 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Copies a 128-row bf16 tile held in shared memory as D/64 128-byte-swizzled
+// boxes of [128 rows][64 columns] into tensor memory as an MMA A operand
+// (lane = row, two consecutive elements per 32-bit column, D/2 columns from
+// `tcol`).  Run by one warpgroup: thread r copies row r.
+template <int D>
+__device__ __forceinline__ void tile_to_tmem(const uint8_t* tile, uint32_t tcol, int r) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) {
+    const uint8_t* box = tile + kb * (128 * 128);
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(r, c));
+      w[4 * c] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+    tmem_st32(tcol + 32 * kb, w);
+  }
+  tmem_st_wait();
+}
+
 }  // namespace sm100
 }  // namespace attn
