@@ -13,6 +13,7 @@
 // rows meet a kept block of that inner tile and, when causal, a key at or
 // below a row.  A unit is `members` consecutive tiles of `osz` rows; inner
 // tiles have `isz` rows.  outer_is_query selects which side is the query.
+// One block per outer unit builds its list in parallel over the inner tiles.
 #include "kernels.h"
 
 namespace attn {
@@ -28,29 +29,50 @@ __device__ __forceinline__ bool range_kept(const uint8_t* __restrict__ mask, int
   return false;
 }
 
-__global__ void tile_lists_kernel(const uint8_t* __restrict__ mask, int n, int causal,
-                                  int outer_is_query, int osz, int members, int isz,
-                                  int* __restrict__ lists, int* __restrict__ counts, int stride) {
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  const int nouter = (n + osz * members - 1) / (osz * members);
-  if (u >= nouter) return;
+// One block per outer unit; its threads take the inner tiles in chunks of
+// kListThreads and write the kept ones in increasing order (ballot within a
+// warp, warp totals through shared memory for the order across warps).
+constexpr int kListThreads = 128;
+
+__global__ void __launch_bounds__(kListThreads)
+tile_lists_kernel(const uint8_t* __restrict__ mask, int n, int causal, int outer_is_query,
+                  int osz, int members, int isz, int* __restrict__ lists,
+                  int* __restrict__ counts, int stride) {
+  __shared__ int warp_tot[kListThreads / 32];
+  const int u = blockIdx.x;
   const int nb = (n + 127) / 128;
   const int ninner = (n + isz - 1) / isz;
-  int cnt = 0;
-  for (int t = 0; t < ninner; ++t) {
-    const int i_lo = t * isz, i_hi = min(n, i_lo + isz);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int base = 0;
+  for (int t0 = 0; t0 < ninner; t0 += kListThreads) {
+    const int t = t0 + (int)threadIdx.x;
     int bits = 0;
-    for (int m = 0; m < members; ++m) {
-      const int o_lo = (u * members + m) * osz;
-      if (o_lo >= n) break;
-      const int o_hi = min(n, o_lo + osz);
-      const bool kept = outer_is_query ? range_kept(mask, nb, o_lo, o_hi, i_lo, i_hi, causal)
-                                       : range_kept(mask, nb, i_lo, i_hi, o_lo, o_hi, causal);
-      if (kept) bits |= 1 << m;
+    if (t < ninner) {
+      const int i_lo = t * isz, i_hi = min(n, i_lo + isz);
+      for (int m = 0; m < members; ++m) {
+        const int o_lo = (u * members + m) * osz;
+        if (o_lo >= n) break;
+        const int o_hi = min(n, o_lo + osz);
+        const bool kept = outer_is_query ? range_kept(mask, nb, o_lo, o_hi, i_lo, i_hi, causal)
+                                         : range_kept(mask, nb, i_lo, i_hi, o_lo, o_hi, causal);
+        if (kept) bits |= 1 << m;
+      }
     }
-    if (bits) lists[(size_t)u * stride + cnt++] = t | (bits << 16);
+    const unsigned kept_lanes = __ballot_sync(0xffffffffu, bits != 0);
+    if (lane == 0) warp_tot[warp] = __popc(kept_lanes);
+    __syncthreads();
+    int off = base, chunk = 0;
+#pragma unroll
+    for (int w = 0; w < kListThreads / 32; ++w) {
+      if (w < warp) off += warp_tot[w];
+      chunk += warp_tot[w];
+    }
+    if (bits) lists[(size_t)u * stride + off + __popc(kept_lanes & ((1u << lane) - 1u))] =
+        t | (bits << 16);
+    __syncthreads();   // warp_tot is rewritten by the next chunk
+    base += chunk;
   }
-  counts[u] = cnt;
+  if (threadIdx.x == 0) counts[u] = base;
 }
 
 }  // namespace
@@ -67,8 +89,8 @@ cudaError_t launch_tile_lists(const uint8_t* mask, int n, int causal, bool outer
   const int ninner = (n + isz - 1) / isz;
   int* lists = buf;
   int* counts = buf + (size_t)nouter * ninner;
-  tile_lists_kernel<<<ceil_div(nouter, 128), 128, 0, st>>>(mask, n, causal, outer_is_query ? 1 : 0,
-                                                          osz, members, isz, lists, counts, ninner);
+  tile_lists_kernel<<<nouter, kListThreads, 0, st>>>(mask, n, causal, outer_is_query ? 1 : 0, osz,
+                                                     members, isz, lists, counts, ninner);
   note_launch();
   return cudaGetLastError();
 }
