@@ -32,7 +32,9 @@
  *     and launch errors only (attn_status_t, 0 = success).  Errors detected
  *     on the device (a bounded wait that ran out) are recorded in a device
  *     status word read by attn_status().
- *   - bf16 path: d in {64, 128, 256}; fp32 path: 1 <= d <= 256.  Any n >= 1.
+ *   - bf16 path: d in {64, 128, 256}; fp32 path: 1 <= d <= 256.  Any n with
+ *     1 <= n <= 8388480 (65535 tiles of 128 rows; ATTN_ERR_UNSUPPORTED above),
+ *     B * H <= 65535.
  *   - Thread-safe: the only global state is the device status word, the
  *     fixed scratch of attn_bwd_noalloc and an atomic launch counter.
  */

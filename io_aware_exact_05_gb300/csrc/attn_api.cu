@@ -22,7 +22,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_common(int B, int H, int n, int d, float scale, int causal) {
   if (B < 1 || H < 1 || n < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
-  if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;   // heads map to grid.y
+  if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;   // heads map to a grid dimension
+  if (n > 65535 * 128) return ATTN_ERR_UNSUPPORTED;            // 128-row tiles map to grid.y
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;

@@ -111,7 +111,14 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, bh = blockIdx.y;   // bh: key/value head (K, V, dK, dV)
+  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
+  // the grid and tiles slowest, longest first, so the long tiles of every
+  // head start early instead of the last heads' long tiles trailing the rest
+  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
+  // head's K and V shared in L2 by CTAs that run together.
+  const bool heads_fast = causal || SPARSE;
+  const int kt = heads_fast ? blockIdx.y : blockIdx.x;
+  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // key/value head (K, V, dK, dV)
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
@@ -491,7 +498,8 @@ int launch_kv(const void* Q, const void* K, const void* V, const void* dO, const
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::BNK), BHkv, gsplit);
+  const int nkt = ceil_div(n, C::BNK);
+  dim3 grid = (causal || SPARSE) ? dim3(BHkv, nkt, gsplit) : dim3(nkt, BHkv, gsplit);
   kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
                                               static_cast<__nv_bfloat16*>(dK),
                                               static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,

@@ -115,10 +115,16 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   constexpr int NOH = D / C::DO;                  // dK/dV column parts (2 for d = 256)
-  const int kt = blockIdx.x;
+  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
+  // the grid and tiles slowest, longest first, so the long tiles of every
+  // head start early instead of the last heads' long tiles trailing the rest
+  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
+  // head's K and V shared in L2 by CTAs that run together.
+  const bool heads_fast = causal || SPARSE;
+  const int kt = heads_fast ? blockIdx.y : blockIdx.x;
   const int oh = (int)blockIdx.z % NOH;          // oh: dK/dV column half (d = 256)
   const int part = (int)blockIdx.z / NOH;        // part of the group (gsplit > 1)
-  const int bh = blockIdx.y;                     // key/value head (K, V, dK, dV)
+  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // key/value head (K, V, dK, dV)
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
@@ -518,9 +524,16 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int ntile = gridDim.x;
-  const int it = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int bh = blockIdx.y;          // query head (Q, dO, dQ, LSE, D)
+  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
+  // the grid and tiles slowest, longest first, so the long tiles of every
+  // head start early instead of the last heads' long tiles trailing the rest
+  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
+  // head's K and V shared in L2 by CTAs that run together.
+  const bool heads_fast = causal || tl.lists != nullptr;
+  const int ntile = heads_fast ? gridDim.y : gridDim.x;
+  const int tile_ix = heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int it = causal ? (ntile - 1 - tile_ix) : tile_ix;
+  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // query head (Q, dO, dQ, LSE, D)
   const int bkv = hm.kv_of(bh);       // key/value head (K, V)
   const int q0 = it * C::BM;
   const int nkv = (n + C::BN - 1) / C::BN;
@@ -744,7 +757,9 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
                              : bwd_kv_kernel<D, DQ, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::BNK), BHkv, (D / C::DO) * gsplit);
+  const int nkt = ceil_div(n, C::BNK);
+  dim3 grid = (causal || tl.lists) ? dim3(BHkv, nkt, (D / C::DO) * gsplit)
+                                   : dim3(nkt, BHkv, (D / C::DO) * gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
@@ -769,7 +784,8 @@ int launch_q(const void* Q, const void* K, const void* V, const void* dO, const 
   auto kern = bwd_q_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::BM), BH);
+  const int ntile = ceil_div(n, C::BM);
+  dim3 grid = (causal || tl.lists) ? dim3(BH, ntile) : dim3(ntile, BH);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, static_cast<__nv_bfloat16*>(dQ),
                                            hm, tl, n, n_pad, scale, scale * 1.4426950408889634f,
                                            causal, ctl);

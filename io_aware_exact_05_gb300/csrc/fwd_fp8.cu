@@ -91,9 +91,16 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int ntile = gridDim.x;
-  const int cta = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
+  // the grid and tiles slowest, longest first, so the long tiles of every
+  // head start early instead of the last heads' long tiles trailing the rest
+  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
+  // head's K and V shared in L2 by CTAs that run together.
+  const bool heads_fast = causal;
+  const int bh = heads_fast ? blockIdx.x : blockIdx.y;
+  const int ntile = heads_fast ? gridDim.y : gridDim.x;
+  const int tile_ix = heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int cta = causal ? (ntile - 1 - tile_ix) : tile_ix;
   const int row0 = cta * (C::QT * C::BM);
   const int nkv = (n + BN - 1) / BN;
   TileRange tr;
@@ -390,7 +397,8 @@ int launch_fwd_fp8(const void* Q8, const void* K8, const void* Vt8, void* O, flo
   if (cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, C::QT * C::BM), BH);
+  const int ntile = ceil_div(n, C::QT * C::BM);
+  dim3 grid = causal ? dim3(BH, ntile) : dim3(ntile, BH);
   fwd_fp8_kernel<<<grid, 384, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE,
                                              descale_q, descale_k, descale_v, n,
                                              scale * 1.4426950408889634f, causal, ctl);

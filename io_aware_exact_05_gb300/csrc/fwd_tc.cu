@@ -124,10 +124,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;        // query head (Q, O, LSE)
+  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
+  // the grid and tiles slowest, longest first, so the long tiles of every
+  // head start early instead of the last heads' long tiles trailing the rest
+  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
+  // head's K and V shared in L2 by CTAs that run together.
+  const bool heads_fast = causal || SPARSE;
+  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // query head (Q, O, LSE)
   const int bkv = GROUPED ? hm.kv_of(bh) : bh;   // key/value head (K, V)
-  const int ntile = gridDim.x;
-  const int cta = causal ? (ntile - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int ntile = heads_fast ? gridDim.y : gridDim.x;
+  const int tile_ix = heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int cta = causal ? (ntile - 1 - tile_ix) : tile_ix;
   const int row0 = cta * (QT * C::BM);
   const int nkv = (n + BN - 1) / BN;
 
@@ -480,7 +487,8 @@ int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE,
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(n, QT * C::BM), BH);
+  const int ntile = ceil_div(n, QT * C::BM);
+  dim3 grid = (causal || tl.lists) ? dim3(BH, ntile) : dim3(ntile, BH);
   const float scale_log2 = scale * 1.4426950408889634f;
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O), LSE, hm, tl,
                                            n, scale_log2, causal, ctl);

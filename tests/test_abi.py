@@ -66,6 +66,7 @@ def test_fwd_argument_checks(L):
     assert _fwd(L, d=0) == 1
     assert _fwd(L, causal=2) == 1
     assert _fwd(L, scale=float("nan")) == 1
+    assert _fwd(L, n=65535 * 128 + 1) == 2     # 128-row tiles map to a 65535-wide grid dimension
     assert _fwd(L, scale=float("inf")) == 1
     assert _fwd(L, dt=7) == 1
     assert _fwd(L, d=96) == 2                # bf16 head dims are 64, 128, 256
