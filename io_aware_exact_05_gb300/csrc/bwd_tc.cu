@@ -19,12 +19,18 @@
 //   dQ_i = dS K        (SS-MMA, A = dS MN-major in smem) -> TMEM, then the
 //                      dQ warpgroup adds scale * dQ_i into an fp32
 //                      accumulator in global memory with vector atomics.
-// For d = 256 the two accumulators already fill the 512 TMEM columns, so
+// Only its d = 256 instances are launched (d = 64 and 128 use the pipelined
+// key-tile kernel of bwd_kv.cuh; the dQ-atomic branches here serve no launch
+// now).  For d = 256 the two accumulators would fill the 512 TMEM columns, so
 // the kernel runs twice per key tile (grid.z = 2), each producing one
-// 128-wide half of dK and dV, and dQ comes from bwd_q_kernel.
+// 128-wide half of dK and dV, and dQ comes from bwd_q_kernel.  K, the A
+// operand of S^T, sits in the TMEM columns this layout leaves free (S^T is
+// then a TS-MMA), which leaves shared memory for two Q/dO stages.
 //
 // bwd_q_kernel -- one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T,
-// dS = P o (dP - D) -> bf16 TMEM, dQ += dS K_j (TS-MMA); no atomics.
+// dS = P o (dP - D) -> bf16 TMEM, dQ += dS K_j (TS-MMA); no atomics.  The dQ
+// pass of every head dim (ATTN_DQ_PASS), and the only dQ path at d = 256,
+// where Q sits in TMEM as the A operand of S.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
