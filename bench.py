@@ -3,11 +3,18 @@
 
 One step = one forward (attn_fwd) and one backward (attn_bwd_preprocess,
 attn_bwd_dkdv, attn_bwd_dq) over the whole workload, inputs resident in HBM.
-Throughput counts the algorithmic FLOPs (forward 4*B*H*n^2*d, backward
-10*B*H*n^2*d, both halved for a causal mask).  Prints one JSON line.
+Grouped-query and block-sparse workloads run attn_fwd_gqa / attn_bwd_gqa and
+attn_fwd_sparse / attn_bwd_sparse (the backward as one call); the e4m3
+workloads run attn_quantize_fp8 on Q, K, V and attn_fwd_fp8.  Throughput
+counts the algorithmic FLOPs (forward 4*B*H*n^2*d, backward 10*B*H*n^2*d,
+both halved for a causal mask; kept entries only for a block pattern).  The
+end-to-end leg copies every step's inputs from pinned host memory and its
+results back, overlapped with the kernels of neighbouring steps.  Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--mode atomic|pass] [--impl ours|reference]
+                  [--mode atomic|pass|auto] [--impl ours|reference]
+                  [--no-cpu-baseline]
 
 Under torchrun each rank runs its own copy of the workload on its GPU (every
 (b, h) head is independent, so there is no collective on the data path:
