@@ -115,10 +115,15 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // the grid and tiles slowest, longest first, so the long tiles of every
   // head start early instead of the last heads' long tiles trailing the rest
   // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
-  // head's K and V shared in L2 by CTAs that run together.
+  // head's K and V shared in L2 by CTAs that run together.  The parts of a
+  // split group count as heads here (hx = part * key/value heads + head), so
+  // the last part's long tiles do not trail either.
   const bool heads_fast = causal || SPARSE;
   const int kt = heads_fast ? blockIdx.y : blockIdx.x;
-  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // key/value head (K, V, dK, dV)
+  const int hx = heads_fast ? blockIdx.x : blockIdx.y;
+  const int nkvh = (heads_fast ? (int)gridDim.x : (int)gridDim.y) / gsplit;
+  const int bh = hx % nkvh;           // key/value head (K, V, dK, dV)
+  const int part = hx / nkvh;         // part of the group
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
@@ -126,12 +131,12 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int cnt = SPARSE ? tl.counts[kt] : nq - i_start;   // query tiles per query head
   auto qtile = [&](int ut) { return SPARSE ? (qlist[ut] & 0xFFFF) : i_start + ut; };
   // The query heads of this key/value head's group are split over gsplit
-  // CTAs (blockIdx.z); iteration u visits query tile i_start + u % cnt of
+  // CTAs (part); iteration u visits query tile i_start + u % cnt of
   // query head qbase + u / cnt, so dK and dV accumulate over this CTA's part
   // of the group (over the whole group when gsplit = 1).  Each role runs an
   // outer loop over its heads and an inner loop over the query tiles.
   const int gper = GROUPED ? hm.group / gsplit : 1;
-  const int qbase = GROUPED ? hm.q_of(bh, (int)blockIdx.z * gper) : bh;
+  const int qbase = GROUPED ? hm.q_of(bh, part * gper) : bh;
   const int total = gper * cnt;
 
   if (threadIdx.x == 0) {
@@ -499,7 +504,7 @@ int launch_kv(const void* Q, const void* K, const void* V, const void* dO, const
       cudaSuccess)
     return ATTN_ERR_CUDA;
   const int nkt = ceil_div(n, C::BNK);
-  dim3 grid = (causal || SPARSE) ? dim3(BHkv, nkt, gsplit) : dim3(nkt, BHkv, gsplit);
+  dim3 grid = (causal || SPARSE) ? dim3(BHkv * gsplit, nkt) : dim3(nkt, BHkv * gsplit);
   kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
                                               static_cast<__nv_bfloat16*>(dK),
                                               static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
