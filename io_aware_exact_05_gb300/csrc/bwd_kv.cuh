@@ -338,16 +338,45 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const bool masked = causal && (k0 + C::BNK - 1 > q0);
         const int qbase = q0 + h * NC;
         float p[NC];
-#pragma unroll
-        for (int c0 = 0; c0 < NC; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(s_addr + c0, rr);
+        if constexpr (D == 64) {
+          // both TMEM loads in flight before one wait, LSE2 four at a time
+          // (every lane reads the same words), column pairs on the paired
+          // fp32 FMA (measured: +3 % at d = 64, -1 % at d = 128)
+          uint32_t* pr = reinterpret_cast<uint32_t*>(p);
+          tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(pr));
+          tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
           tmem_ld_wait();
+          reg_fence<NC>(*reinterpret_cast<uint32_t(*)[NC]>(pr));
+          const float4* l4 = reinterpret_cast<const float4*>(lse2);
+          const float2 c2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
-            if (masked && key > qbase + c0 + i) v = 0.f;
-            p[c0 + i] = v;
+          for (int i4 = 0; i4 < NC / 4; ++i4) {
+            const float4 L = l4[i4];
+            const float2 x0 = __ffma2_rn(make_float2(p[4 * i4], p[4 * i4 + 1]), c2, make_float2(-L.x, -L.y));
+            const float2 x1 = __ffma2_rn(make_float2(p[4 * i4 + 2], p[4 * i4 + 3]), c2,
+                                         make_float2(-L.z, -L.w));
+            p[4 * i4] = ex2(x0.x);
+            p[4 * i4 + 1] = ex2(x0.y);
+            p[4 * i4 + 2] = ex2(x1.x);
+            p[4 * i4 + 3] = ex2(x1.y);
+          }
+          if (masked) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+              if (key > qbase + c) p[c] = 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < NC; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(s_addr + c0, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
+              if (masked && key > qbase + c0 + i) v = 0.f;
+              p[c0 + i] = v;
+            }
           }
         }
 #pragma unroll
@@ -369,11 +398,30 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           uint32_t rr[32];
           tmem_ld32(dp_addr + c0, rr);
           tmem_ld_wait();
+          if constexpr (D == 64) {   // D four at a time, paired fp32 subtract and multiply
+            const float4* d4 = reinterpret_cast<const float4*>(dd + c0);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            ds[c0 / 2 + i] =
-                pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
-                            p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 Dq = d4[i4];
+              const int c = c0 + 4 * i4;
+              const float2 x0 = __fmul2_rn(
+                  make_float2(p[c], p[c + 1]),
+                  __fadd2_rn(make_float2(__uint_as_float(rr[4 * i4]), __uint_as_float(rr[4 * i4 + 1])),
+                             make_float2(-Dq.x, -Dq.y)));
+              const float2 x1 = __fmul2_rn(
+                  make_float2(p[c + 2], p[c + 3]),
+                  __fadd2_rn(make_float2(__uint_as_float(rr[4 * i4 + 2]), __uint_as_float(rr[4 * i4 + 3])),
+                             make_float2(-Dq.z, -Dq.w)));
+              ds[c0 / 2 + 2 * i4] = pack_bf16x2(x0.x, x0.y);
+              ds[c0 / 2 + 2 * i4 + 1] = pack_bf16x2(x1.x, x1.y);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              ds[c0 / 2 + i] =
+                  pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
+                              p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
+          }
         }
         tc_fence_before();
         // dS^T over dO(u) must wait until dV(u) has read dO; a separate
