@@ -257,8 +257,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       auto last_user = [&](int t, int j) { return QT == 1 || t == 1 || j > ti.last1; };
       bool ok = mbar_wait_warp(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
       if (C::Q_IN_TMEM) ok = ok && mbar_wait_warp(bar(B_QC), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      // SPARSE: a unit whose list entry is not kept for its tile ("dropped")
+      // gets no MMAs; its waits and commits stay, so every barrier phase is
+      // the same as with the MMAs (a commit with nothing new completes when
+      // the earlier MMAs have).  Bit k & 1 of drop_s remembers S(k)'s flag for
+      // PV(k); bit t of o_init says tile t's O holds a first PV already.
+      uint32_t drop_s = 0, o_init = 0;
+      auto dropped_unit = [&](const Unit& u, int ent) {
+        return SPARSE && !((ent >> (16 + u.t)) & 1);
+      };
       // S(k) = Q_t K_j^T into S slot k & 1
-      auto issue_s = [&](int k) -> bool {
+      auto issue_s = [&](int k, int ent) -> bool {
         const Unit u = unit_at<QT>(k, ti);
         const int s = u.j % C::KSTK;
         const uint32_t qb = q_lo + u.t * (C::Q_BYTES >> 4), kb = k_lo + s * (C::KV_BYTES >> 4);
@@ -266,9 +275,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (!mbar_wait_warp(bar(B_KF + s), (u.j / C::KSTK) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
             return false;
         }
+        const bool drop = dropped_unit(u, ent);
+        drop_s = (drop_s & ~(1u << (k & 1))) | ((uint32_t)drop << (k & 1));
         tc_fence_after();
 #pragma unroll
         for (int b = 0; b < C::NKB; ++b) {   // one 64-wide column box of Q and K per group
+          if (drop) break;
           uint32_t alo[4], blo[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -285,28 +297,34 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (last_user(u.t, u.j)) tc_commit(bar(B_KE + s));
         return true;
       };
-      if (ok && total > 0) ok = issue_s(0);
-      if (ok && total > 1) ok = issue_s(1);
+      auto entry_of = [&](int k) { return SPARSE ? slist[unit_at<QT>(k, ti).j] : 0; };
+      if (ok && total > 0) ok = issue_s(0, entry_of(0));
+      if (ok && total > 1) ok = issue_s(1, entry_of(1));
       for (int k = 0; ok && k < total; ++k) {
         const Unit u = unit_at<QT>(k, ti);
         const int s = u.j % C::KSTV;
         const uint32_t vb = v_lo + s * (C::KV_BYTES >> 4);
         const uint32_t pa = tmem + C::S_COL + (k & 1) * BN;   // P: bf16 pairs, BN/2 columns
+        const int ent2 = (SPARSE && k + 2 < total) ? entry_of(k + 2) : 0;   // load before the wait
         if (!mbar_wait_warp(bar(B_PF + (k & 1)), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
         if (first_user(u.t, u.j)) {
           if (!mbar_wait_warp(bar(B_VF + s), (u.j / C::KSTV) & 1, abort_flag, ctl, SITE_FWD_V_FULL)) break;
         }
         tc_fence_after();
+        const bool drop_pv = SPARSE && ((drop_s >> (k & 1)) & 1);
 #pragma unroll
         for (int b = 0; b < BN / 64; ++b) {   // 64 keys (4 MMAs of K = 16) per group
+          if (drop_pv) break;
           uint32_t blo[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) blo[i] = vb + (4 * b + i) * (2048 / 16);
-          mma_ts_x4(tmem + C::O_COL + u.t * D, pa + 32 * b, blo, HI, idesc_o, (u.j > 0 || b > 0));
+          const bool acc = SPARSE ? (((o_init >> u.t) & 1) || b > 0) : (u.j > 0 || b > 0);
+          mma_ts_x4(tmem + C::O_COL + u.t * D, pa + 32 * b, blo, HI, idesc_o, acc);
         }
+        if (SPARSE && !drop_pv) o_init |= 1u << u.t;
         if (!pv_implied(u.t, u.j, ti)) tc_commit(bar(B_OD + u.t));
         if (last_user(u.t, u.j)) tc_commit(bar(B_VE + s));
-        if (k + 2 < total) ok = issue_s(k + 2);
+        if (k + 2 < total) ok = issue_s(k + 2, ent2);
       }
       if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         tc_commit(bar(B_DRAIN));
@@ -343,61 +361,63 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       ok = mbar_wait(bar(B_SF + slot), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_S_FULL);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t sa = tmem + lane_off + C::S_COL + slot * BN;
-      // all BN columns of this row: issue every TMEM load, then wait once
-      uint32_t sr[BN];
+      // SPARSE: an entry kept only for the other tile of the CTA ("dropped")
+      // got no S or PV MMA; its step keeps only the barrier phases
+      const bool drop = SPARSE && !((ent >> (16 + t)) & 1);
+      float alpha = 1.0f, m_new = m;
+      if (!drop) {
+        tc_fence_after();
+        const uint32_t sa = tmem + lane_off + C::S_COL + slot * BN;
+        // all BN columns of this row: issue every TMEM load, then wait once
+        uint32_t sr[BN];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32)
-        tmem_ld32(sa + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
-      tmem_ld_wait();
-      reg_fence<BN>(sr);
-      float* s = reinterpret_cast<float*>(sr);
-      const int col0 = (SPARSE ? (ent & 0xFFFF) : j) * BN;
-      // SPARSE: an entry not kept for this tile (kept only for the other
-      // tile of the CTA) is masked whole
-      const bool dropped = SPARSE && !((ent >> (16 + t)) & 1);
-      const bool need_mask =
-          dropped || (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
-      if (need_mask) {
-        const int lim = dropped ? col0 : causal ? min(n, row + 1) : n;   // columns < lim are kept
+        for (int c0 = 0; c0 < BN; c0 += 32)
+          tmem_ld32(sa + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+        tmem_ld_wait();
+        reg_fence<BN>(sr);
+        float* s = reinterpret_cast<float*>(sr);
+        const int col0 = (SPARSE ? (ent & 0xFFFF) : j) * BN;
+        const bool need_mask = (col0 + BN > n) || (causal && col0 + BN - 1 > row0 + t * C::BM);
+        if (need_mask) {
+          const int lim = causal ? min(n, row + 1) : n;   // columns < lim are kept
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (col0 + c >= lim) s[c] = -INFINITY;
-      }
-      // row maximum: three-input maxima in four independent chains
-      float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int c = 4; c < BN; c += 2) mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], s[c], s[c + 1]);
-      const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-      const float m_cand = mx * scale_log2;
-      const float m_new = (m_cand > m + 8.0f) ? m_cand : m;
-      // SPARSE: a row can have no kept score yet (m_new = -inf); exponents are
-      // then taken against 0, so P = 0 and alpha = 0 instead of NaN
-      const float m_base = (SPARSE && m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_base);   // 0 on the first tile (m = -inf)
-      // exponents and row sum on column pairs (paired fp32 FMA and add)
-      const float2 c2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-m_base, -m_base);
-      float2 rs4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = __ffma2_rn(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
-          const float2 p = make_float2(ex2(x.x), ex2(x.y));
-          rs4[i & 3] = __fadd2_rn(rs4[i & 3], p);
-          pk[i] = pack_bf16x2(p.x, p.y);
+          for (int c = 0; c < BN; ++c)
+            if (col0 + c >= lim) s[c] = -INFINITY;
         }
-        tmem_st16(pa + c0 / 2, pk);
+        // row maximum: three-input maxima in four independent chains
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int c = 4; c < BN; c += 2) mx4[(c >> 1) & 3] = max3f(mx4[(c >> 1) & 3], s[c], s[c + 1]);
+        const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+        const float m_cand = mx * scale_log2;
+        m_new = (m_cand > m + 8.0f) ? m_cand : m;
+        // SPARSE: a row can have no kept score yet (m_new = -inf); exponents are
+        // then taken against 0, so P = 0 and alpha = 0 instead of NaN
+        const float m_base = (SPARSE && m_new == -INFINITY) ? 0.f : m_new;
+        alpha = ex2(m - m_base);   // 0 on the first tile (m = -inf)
+        // exponents and row sum on column pairs (paired fp32 FMA and add)
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_base, -m_base);
+        float2 rs4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        const uint32_t pa = sa;   // P overwrites the first BN/2 columns of the slot
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
+            const float2 p = make_float2(ex2(x.x), ex2(x.y));
+            rs4[i & 3] = __fadd2_rn(rs4[i & 3], p);
+            pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(pa + c0 / 2, pk);
+        }
+        const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
+        const float rs = rs2.x + rs2.y;
+        tmem_st_wait();
+        l = l * alpha + rs;
       }
-      const float2 rs2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
-      const float rs = rs2.x + rs2.y;
-      tmem_st_wait();
-      l = l * alpha + rs;
       // PV of step j-1 must be done before O is rescaled.  It is when its
       // completion was implied by the S wait above; otherwise wait for its
       // own commit (every committed phase is waited for, so a parity wait
@@ -409,7 +429,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         ++odc;
       }
       // Rescale this row of O when its kept maximum moved.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // dropped: alpha = 1
         tc_fence_after();
         const uint32_t oa = tmem + lane_off + C::O_COL + t * D;
 #pragma unroll 1
@@ -438,7 +458,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv = (SPARSE && l == 0.f) ? 0.f : 1.f / l;   // no kept score: O = 0
+        // SPARSE, no kept score in this row: O = 0 (its TMEM columns may never
+        // have been written, when every entry was dropped for this tile)
+        const bool zero = SPARSE && l == 0.f;
+        const float inv = zero ? 0.f : 1.f / l;
         const uint32_t oa = tmem + lane_off + C::O_COL + t * D;
         const size_t obase = ((size_t)bh * n + row) * D;
 #pragma unroll 1
@@ -449,7 +472,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (row < n) {
             float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
+            for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : __uint_as_float(rr[i]);
             store_row_bf16(O + obase + c0, v, inv);
           }
         }
