@@ -521,7 +521,10 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    if (lead) bulk_wait_all();
+    // The staging buffers must be read before the CTA exits; the reduce-adds
+    // themselves complete on their own (the kernel's end orders them before
+    // any later work), so the next CTA on this SM starts while they drain.
+    if (lead) bulk_wait_read_all();
   }
 
   tc_fence_before();
