@@ -475,7 +475,7 @@ def run_ours(args, w):
             "dtype": "bf16", "data": "synthetic",
             "pct_of_peak": 100.0 * value / ws_n / peak,
             "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "n": w.n,
-                       "d": w.d, "causal": w.causal, "dq_mode": args.mode,
+                       "d": w.d, "causal": w.causal, "dq_mode": mode_used,
                        "block_pattern": ({"window": w.sparse[0], "global": w.sparse[1],
                                           "random": w.sparse[2], "block": 128}
                                          if w.sparse else None),
@@ -649,7 +649,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", default="atomic", choices=["atomic", "pass", "auto"])
+    ap.add_argument("--mode", default="auto", choices=["atomic", "pass", "auto"],
+                    help="dQ mode; auto: atomic for d <= 128, the dQ pass above")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
