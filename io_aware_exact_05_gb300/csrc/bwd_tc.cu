@@ -22,10 +22,11 @@
 // Only its d = 256 instances are launched (d = 64 and 128 use the pipelined
 // key-tile kernel of bwd_kv.cuh; the dQ-atomic branches here serve no launch
 // now).  For d = 256 the two accumulators would fill the 512 TMEM columns, so
-// the kernel runs twice per key tile (grid.z = 2), each producing one
-// 128-wide half of dK and dV, and dQ comes from bwd_q_kernel.  K, the A
-// operand of S^T, sits in the TMEM columns this layout leaves free (S^T is
-// then a TS-MMA), which leaves shared memory for two Q/dO stages.
+// two neighbouring CTAs share each key tile: one accumulates all of dV (it
+// needs S^T only: no dP^T, no dS^T, no V), the other all of dK (S^T, dP^T,
+// dS^T), and dQ comes from bwd_q_kernel.  K, the A operand of S^T, sits in
+// the TMEM columns this layout leaves free (S^T is then a TS-MMA), which
+// leaves shared memory for two Q/dO stages.
 //
 // bwd_q_kernel -- one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T,
 // dS = P o (dP - D) -> bf16 TMEM, dQ += dS K_j (TS-MMA); no atomics.  The dQ
@@ -60,7 +61,12 @@ template <int D, bool DQ>
 struct KvCfg {
   static constexpr int BNK = 128;                    // keys per CTA (TMEM lanes)
   static constexpr int BM = (D == 256) ? 64 : 128;   // queries per iteration
-  static constexpr int DO = (D == 256) ? 128 : D;    // dK/dV columns per CTA
+  static constexpr int DO = D;                       // accumulator columns (all of d)
+  // d = 256: dV and dK of a key tile would take all 512 TMEM columns, so two
+  // CTAs share a key tile, one accumulating dV (needs S only) and one dK
+  // (needs S and dP); each recomputes S, only the dK CTA computes dP
+  static constexpr bool SPLIT_OUT = (D == 256);
+  static constexpr int NOUT = SPLIT_OUT ? 2 : 1;     // CTAs per key tile
   static constexpr int STG = 2;
   // d = 256: K (the A operand of S^T = K Q^T, constant for the CTA) lives in
   // tensor memory, which frees the shared memory of a second Q/dO stage
@@ -81,14 +87,14 @@ struct KvCfg {
   static constexpr uint32_t DS_BYTES = (WITH_DQ && !DS_ALIAS) ? BM * BNK * 2 : 0;
   static constexpr uint32_t BAR_OFF = DS_OFF + DS_BYTES;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
-  // TMEM columns
+  // TMEM columns (SPLIT_OUT: the CTA's one accumulator at column 0)
   static constexpr int DV_COL = 0;
-  static constexpr int DK_COL = DO;
-  static constexpr int S_COL = 2 * DO;
-  static constexpr int DP_COL = 2 * DO + BM;
-  static constexpr int K_COL = 2 * DO + 2 * BM;       // K as A operand (K_IN_TMEM)
+  static constexpr int DK_COL = SPLIT_OUT ? 0 : DO;
+  static constexpr int S_COL = SPLIT_OUT ? DO : 2 * DO;
+  static constexpr int DP_COL = S_COL + BM;
+  static constexpr int K_COL = S_COL + 2 * BM;        // K as A operand (K_IN_TMEM)
   static constexpr int NTHREADS = WITH_DQ ? 512 : 384;
-  static_assert(2 * DO + 2 * BM + (K_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
+  static_assert(S_COL + 2 * BM + (K_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
   static_assert(!K_IN_TMEM || (KV_BYTES <= STAGE && !DQ), "K in tensor memory: no dQ here");
   static_assert(!WITH_DQ || (BM == 128 && D <= BM), "dQ tile reuses the S columns");
   static_assert(!(D == 256 && DQ), "d = 256 takes dQ from the query-tile kernel");
@@ -120,17 +126,20 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  constexpr int NOH = D / C::DO;                  // dK/dV column parts (2 for d = 256)
   // Causal or block-sparse (tiles of unequal length): heads vary fastest in
   // the grid and tiles slowest, longest first, so the long tiles of every
   // head start early instead of the last heads' long tiles trailing the rest
   // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
   // head's K and V shared in L2 by CTAs that run together.
+  // The two CTAs of a key tile (SPLIT_OUT) are neighbours in the grid.
   const bool heads_fast = causal || SPARSE;
   const int kt = heads_fast ? blockIdx.y : blockIdx.x;
-  const int oh = (int)blockIdx.z % NOH;          // oh: dK/dV column half (d = 256)
-  const int part = (int)blockIdx.z / NOH;        // part of the group (gsplit > 1)
-  const int bh = heads_fast ? blockIdx.x : blockIdx.y;   // key/value head (K, V, dK, dV)
+  const int hx = heads_fast ? blockIdx.x : blockIdx.y;
+  const int oh = hx % C::NOUT;                   // SPLIT_OUT: 0 accumulates dV, 1 dK
+  const int bh = hx / C::NOUT;                   // key/value head (K, V, dK, dV)
+  const int part = (int)blockIdx.z;              // part of the group (gsplit > 1)
+  const bool want_dv = !C::SPLIT_OUT || oh == 0;
+  const bool want_dk = !C::SPLIT_OUT || oh == 1;
   const int k0 = kt * C::BNK;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
@@ -178,11 +187,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp < 4) {
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer
-      mbar_expect_tx(bar(K_KV), 2 * C::KV_BYTES);
+      mbar_expect_tx(bar(K_KV), (want_dk ? 2 : 1) * C::KV_BYTES);   // V only for dP
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
         tma_load_3d(sb + C::K_LOAD_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
-        tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
+        if (want_dk)
+          tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
       }
       int issued_last[2] = {-1, -1};
       bool go = true;
@@ -252,36 +262,41 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                    sdesc_sw128(qa + qoff, 16, 1024), id_s, kk > 0);
         }
         tc_commit(bar(K_SF));
+        if (want_dk) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t voff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
-          const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::DP_COL, sdesc_sw128(va + voff, 16, 1024), sdesc_sw128(ga + goff, 16, 1024),
-                 id_s, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t voff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
+            const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::DP_COL, sdesc_sw128(va + voff, 16, 1024),
+                   sdesc_sw128(ga + goff, 16, 1024), id_s, kk > 0);
+          }
+          tc_commit(bar(K_DPF));
         }
-        tc_commit(bar(K_DPF));
         // dV += P^T dO   (contraction over the BM queries of this tile)
-        if (!(ok = mbar_wait_warp(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
-        tc_fence_after();
-        const uint32_t boff = oh * 2 * (C::BM * 128);   // first dO/Q column box of this half
+        if (want_dv) {
+          if (!(ok = mbar_wait_warp(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
-          const int h = (16 * kk) / (C::BM / 2);
-          const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
-                 sdesc_sw128(ga + boff + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          for (int kk = 0; kk < C::BM / 16; ++kk) {
+            // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
+            const int h = (16 * kk) / (C::BM / 2);
+            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
+            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
+                   sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          }
+          if (C::DS_ALIAS) tc_commit(bar(K_DVD));
         }
-        if (C::DS_ALIAS) tc_commit(bar(K_DVD));
         // dK += dS^T Q ; dQ_i = dS K
-        if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
-        tc_fence_after();
+        if (want_dk) {
+          if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const int h = (16 * kk) / (C::BM / 2);
-          const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + acol,
-                 sdesc_sw128(qa + boff + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          for (int kk = 0; kk < C::BM / 16; ++kk) {
+            const int h = (16 * kk) / (C::BM / 2);
+            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
+            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + acol,
+                   sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          }
         }
         if (C::WITH_DQ) {
           const uint32_t dsa = C::DS_ALIAS ? ga : (sb + C::DS_OFF);
@@ -347,16 +362,19 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             p[c0 + i] = v;
           }
         }
+        if (want_dv) {   // P^T in bf16 over S^T: the A operand of dV
 #pragma unroll
-        for (int c0 = 0; c0 < NC; c0 += 32) {
-          uint32_t pk[16];
+          for (int c0 = 0; c0 < NC; c0 += 32) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
-          tmem_st16(s_addr + c0 / 2, pk);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(p[c0 + 2 * i], p[c0 + 2 * i + 1]);
+            tmem_st16(s_addr + c0 / 2, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(K_PR));
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(K_PR));
+        if (!want_dk) continue;   // SPLIT_OUT, dV CTA: no dP, no dS
         ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -400,19 +418,23 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_arrive(bar(K_DSR));
       }
     }
-    // ---- epilogue: half 0 writes dV, half 1 writes dK (scaled)
+    // ---- epilogue: SPLIT_OUT: warpgroup h writes columns [h d/2, (h+1) d/2)
+    // of this CTA's output; otherwise half 0 writes dV and half 1 dK (scaled)
     if (ok) {
       ok = mbar_wait(bar(K_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      const uint32_t src = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      const size_t off = ((size_t)bh * n + key) * D + oh * C::DO;
-      const float mul = h == 0 ? 1.f : scale;
-      float* acc = GROUPED ? (h == 0 ? dVacc : dKacc) : nullptr;   // set when the group is split
+      const bool out_dv = C::SPLIT_OUT ? want_dv : h == 0;
+      constexpr int W = C::SPLIT_OUT ? D / 2 : C::DO;   // columns of this warpgroup
+      const int c_first = C::SPLIT_OUT ? h * W : 0;
+      const uint32_t src = tmem + lane_off + (out_dv ? C::DV_COL : C::DK_COL) + c_first;
+      const size_t off = ((size_t)bh * n + key) * D + c_first;
+      const float mul = out_dv ? 1.f : scale;
+      float* acc = GROUPED ? (out_dv ? dVacc : dKacc) : nullptr;   // set when the group is split
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::DO; c0 += 32) {
+      for (int c0 = 0; c0 < W; c0 += 32) {
         uint32_t rr[32];
         tmem_ld32(src + c0, rr);
         tmem_ld_wait();
@@ -428,7 +450,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                          mul * __uint_as_float(rr[i + 1]), mul * __uint_as_float(rr[i + 2]),
                          mul * __uint_as_float(rr[i + 3]));
           } else {
-            store32_bf16((h == 0 ? dV : dK) + off + c0, rr, mul);
+            store32_bf16((out_dv ? dV : dK) + off + c0, rr, mul);
           }
         }
       }
@@ -764,8 +786,8 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const int nkt = ceil_div(n, C::BNK);
-  dim3 grid = (causal || tl.lists) ? dim3(BHkv, nkt, (D / C::DO) * gsplit)
-                                   : dim3(nkt, BHkv, (D / C::DO) * gsplit);
+  dim3 grid = (causal || tl.lists) ? dim3(BHkv * C::NOUT, nkt, gsplit)
+                                   : dim3(nkt, BHkv * C::NOUT, gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
