@@ -246,7 +246,9 @@ ATTN_API int attn_bwd_gqa(const void* Q, const void* K, const void* V, const voi
  *                        every dQ share into the workspace accumulator.
  *   attn_bwd_dq          ATTN_DQ_ATOMIC: converts the accumulator to dQ;
  *                        ATTN_DQ_PASS: the query-tile kernel computes dQ.
- * Pointers not used by a stage may be NULL.
+ * Pointers not used by a stage may be NULL.  attn_bwd_dkdv and attn_bwd_dq
+ * are bf16 only: the fp32 kernels read LSE, which these stages do not take,
+ * so ATTN_F32 returns ATTN_ERR_INVALID_ARG there (attn_bwd runs fp32).
  */
 ATTN_API int attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
              int B, int H, int n, int d, attn_dtype dtype, int causal,

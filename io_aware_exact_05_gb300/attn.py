@@ -91,6 +91,8 @@ def lib():
             L.attn_bwd_dkdv.restype = i
             L.attn_bwd_dq.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
             L.attn_bwd_dq.restype = i
+            L.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
+            L.attn_bwd_noalloc.restype = i
             L.attn_mat_workspace_size.argtypes = [i, i, i, i]
             L.attn_mat_workspace_size.restype = sz
             L.attn_mat_fwd.argtypes = [vp] * 5 + [i, i, i, i, f, i, vp, sz, vp]
@@ -195,6 +197,17 @@ def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, mode=ATTN_DQ_AUTO,
                         int(bool(causal)), int(mode), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_bwd")
+
+
+def attn_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, scale, causal, stream=None):
+    """The backward without a workspace: its row statistics live in a fixed
+    device array inside the library (dQ by the query-tile pass).  Calls that
+    overlap on the GPU share that array, so keep them on one stream."""
+    B, H, n, d = _shape(Q)
+    rc = lib().attn_bwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
+                                _ptr(dQ), _ptr(dK), _ptr(dV), B, H, n, d, _dtype_code(Q),
+                                float(scale), int(bool(causal)), _stream(stream))
+    _check(rc, "attn_bwd_noalloc")
 
 
 def _kv_heads(Q, K):

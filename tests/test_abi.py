@@ -119,6 +119,43 @@ def test_bwd_argument_checks(L):
     assert L.attn_bwd(*bad, 1, 2, 256, 128, 0, 0.1, 1, 0, ws, 1 << 30, None) == 1
 
 
+def test_backward_stage_argument_checks(L):
+    """attn_bwd_preprocess / attn_bwd_dkdv / attn_bwd_dq check like attn_bwd,
+    before any launch, and a rejected call enqueues nothing."""
+    ws = ctypes.c_void_p(1 << 24)
+    before = L.attn_launch_count()
+
+    def pre(*, d=128, dt=0, mode=0, wsb=1 << 30, wsp=ws, causal=1, ptr=FAKE):
+        return L.attn_bwd_preprocess(ptr, FAKE, FAKE, 1, 2, 256, d, dt, causal, mode, wsp, wsb,
+                                     None)
+
+    def kv(*, d=128, dt=0, mode=0, wsb=1 << 30, wsp=ws, scale=0.1, ptr=FAKE):
+        return L.attn_bwd_dkdv(ptr, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, d, dt, scale, 1,
+                               mode, wsp, wsb, None)
+
+    def dq(*, d=128, dt=0, mode=0, wsb=1 << 30, wsp=ws, scale=0.1, ptr=FAKE, qptr=FAKE):
+        # ptr: dQ (always used); qptr: Q (read only by the dQ pass)
+        return L.attn_bwd_dq(qptr, FAKE, FAKE, FAKE, ptr, 1, 2, 256, d, dt, scale, 1, mode, wsp,
+                             wsb, None)
+
+    for f in (pre, kv, dq):
+        assert f(ptr=ctypes.c_void_p(0)) == 1                 # null tensor
+        assert f(ptr=ctypes.c_void_p((1 << 20) + 8)) == 1     # not 16-byte aligned
+        assert f(mode=9) == 1
+        assert f(dt=5) == 1
+        assert f(d=96) == 2                                   # bf16 head dims: 64, 128, 256
+        assert f(d=256, mode=1) == 2                          # atomic dQ needs d <= 128
+        assert f(dt=1, d=300) == 2                            # fp32: d <= 256
+        assert f(wsb=16) == 3
+        assert f(wsp=ctypes.c_void_p(0)) == 3
+        assert f(wsp=ctypes.c_void_p((1 << 24) + 16)) == 3    # not 256-byte aligned
+    assert pre(causal=2) == 1
+    assert kv(scale=float("inf")) == 1 and dq(scale=float("nan")) == 1
+    assert dq(mode=2, qptr=ctypes.c_void_p(0)) == 1          # the dQ pass reads Q
+    assert dq(dt=1) == 1 and kv(dt=1) == 1                   # fp32: attn_bwd only
+    assert L.attn_launch_count() == before
+
+
 def test_gqa_argument_checks(L):
     def fwd(H=4, Hkv=2, d=64):
         return L.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, H, Hkv, 128, d, 0, 0.125, 0, None)

@@ -26,11 +26,7 @@ def _noalloc():
 
     if not os.path.exists(attn.lib_path()):
         build()
-    f = attn.lib().attn_bwd_noalloc
-    f.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
-                                                                 ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    return f
+    return attn.lib().attn_bwd_noalloc   # argument types set by the binding
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
