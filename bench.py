@@ -266,6 +266,15 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def dq_mode_used(mode, d):
+    """The dQ mode a bf16 backward runs: "auto" is the reduce-add from the
+    key-tile kernel for d <= 128 and the separate dQ pass above (the library's
+    own rule)."""
+    if mode != "auto":
+        return mode
+    return "atomic" if d <= 128 else "pass"
+
+
 def traffic_per_launch(w):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source and this workload."""
@@ -354,7 +363,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     mode = {"atomic": attn.ATTN_DQ_ATOMIC, "pass": attn.ATTN_DQ_PASS,
             "auto": attn.ATTN_DQ_AUTO}[args.mode]
-    mode_used = args.mode if args.mode != "auto" else ("atomic" if w.d <= 128 else "pass")
+    mode_used = dq_mode_used(args.mode, w.d)
     wr = rank_workload(w, rank)
     x = make_inputs(wr)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))

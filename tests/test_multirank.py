@@ -76,6 +76,13 @@ def test_whole_job_rate_and_single_rank_identity():
     assert b.rank_workload(w, 3).with_shape(seed=w.seed) == w
 
 
+def test_dq_mode_default_follows_the_library_rule():
+    b = _bench()
+    assert b.dq_mode_used("auto", 64) == b.dq_mode_used("auto", 128) == "atomic"
+    assert b.dq_mode_used("auto", 256) == "pass"
+    assert b.dq_mode_used("pass", 128) == "pass" and b.dq_mode_used("atomic", 64) == "atomic"
+
+
 def test_reference_arm_under_torchrun_prints_once():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
