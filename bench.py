@@ -9,12 +9,14 @@ workloads run attn_quantize_fp8 on Q, K, V and attn_fwd_fp8.  Throughput
 counts the algorithmic FLOPs (forward 4*B*H*n^2*d, backward 10*B*H*n^2*d,
 both halved for a causal mask; kept entries only for a block pattern).  The
 end-to-end leg copies every step's inputs from pinned host memory and its
-results back, overlapped with the kernels of neighbouring steps.  Prints one
+results back, overlapped with the kernels of neighbouring steps.  A sustained
+leg then repeats the step for a few seconds, so that the clocks settle under
+the power cap, and reports it against the sustained tensor peak.  Prints one
 JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--mode atomic|pass|auto] [--impl ours|reference]
-                  [--no-cpu-baseline]
+                  [--no-cpu-baseline] [--sustain-s SECONDS]
 
 Under torchrun each rank runs its own copy of the workload on its GPU (every
 (b, h) head is independent, so there is no collective on the data path:
@@ -49,6 +51,10 @@ METRIC_FP8 = ("attention fwd TFLOP/s with e4m3 Q/K/V/P (bf16 inputs quantised on
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "b2h16_n8k_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# end-to-end steps: enough that the pipeline's fill and drain (one step's
+# input copy before the first kernel, one result copy after the last) are a
+# small share of the region
+E2E_MIN_STEPS = 24
 
 
 def peaks():
@@ -350,6 +356,33 @@ def e2e_ms_pipelined(step, bufsets, hx, ho, steps, st):
     return t0.elapsed_time(t1)
 
 
+def sustained_leg(step, bufs, ev, kernel_stage, seconds, st, gpu_index):
+    """Repeat the step back to back for at least `seconds` of wall time after
+    the timed region (the clocks settle under the power cap over seconds).
+    Steps run in chunks of len(ev), each step with its stage events; returns
+    the mean step time, the mean time of stage `kernel_stage` and the clocks
+    sampled over the leg."""
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    steps, total_ms, kern_ms = 0, 0.0, 0.0
+    wall0 = time.perf_counter()
+    while time.perf_counter() - wall0 < seconds:
+        t0.record(st)
+        for e in ev:
+            step(bufs, e)
+        t1.record(st)
+        torch.cuda.synchronize()
+        total_ms += t0.elapsed_time(t1)
+        kern_ms += sum(e[kernel_stage].elapsed_time(e[kernel_stage + 1]) for e in ev)
+        steps += len(ev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    return {"steps": steps, "wall_s": wall, "ms_per_step": total_ms / steps,
+            "kernel_ms": kern_ms / steps, "clocks": clk}
+
+
 def run_ours(args, w):
     from io_aware_exact_05_gb300 import attn
 
@@ -457,7 +490,7 @@ def run_ours(args, w):
           for n in ("o", "lse", "dq", "dk", "dv")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(4, args.steps // 4)
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
     e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
@@ -468,6 +501,14 @@ def run_ours(args, w):
     rc = attn.attn_status()
     if rc:
         raise RuntimeError("device status after the end-to-end run: " + attn.attn_strerror(rc))
+
+    # ---- sustained: the same step back to back for seconds, after the timed region
+    sus = None
+    if args.sustain_s > 0:
+        sus = sustained_leg(step, buf0, ev, 2, args.sustain_s, st, local)
+        rc = attn.attn_status()
+        if rc:
+            raise RuntimeError("device status after the sustained run: " + attn.attn_strerror(rc))
 
     if rank == 0:
         kv_ms = stage_ms[2]
@@ -510,6 +551,18 @@ def run_ours(args, w):
             "gpu_launches": launches,
             "clocks": clk,
         }
+        if sus is not None:
+            speak = float(pk.get("bf16_tflops_sustained", peak))
+            k_ach = kv_flops / (sus["kernel_ms"] * 1e-3) / 1e12
+            line["sustained"] = {
+                "what": "the step repeated back to back for %.1f s after the timed region "
+                        "(%d steps), CUDA events per step" % (sus["wall_s"], sus["steps"]),
+                "value": per_step / (sus["ms_per_step"] * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": sus["ms_per_step"],
+                "kernel": line["roofline"]["kernel"], "kernel_ms": sus["kernel_ms"],
+                "achieved": k_ach, "peak": speak, "frac": k_ach / speak,
+                "peak_source": "%s bf16_tflops_sustained" % src,
+                "clocks": sus["clocks"]}
         if not args.no_cpu_baseline and ws_n == 1:
             line["cpu_baseline"] = time_oracle(w, x)
         print(json.dumps(line), flush=True)
@@ -596,7 +649,7 @@ def run_fp8(args, w):
           for n in ("o", "lse")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(4, args.steps // 4)
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
     e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
@@ -662,6 +715,9 @@ def main():
                     help="dQ mode; auto: atomic for d <= 128, the dQ pass above")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps after the timed region, reported "
+                         "against the sustained peak (0: skip)")
     args = ap.parse_args()
     w = workload(args.workload)
     if args.impl == "reference":

@@ -282,7 +282,9 @@ ATTN_API int attn_bwd_dq(const void* Q, const void* K, const void* V,
  *     streams, or two threads without ordering) race: keep them on one stream
  *     or synchronise in between.  Nothing in the array needs to start at zero.
  *   - The first call on each device looks up the array's address on that
- *     device; make that first call before capturing any stream.
+ *     device; make that first call before capturing any stream.  The address
+ *     is kept per CUDA context: after cudaDeviceReset, or under another
+ *     context made current on the device, the next call looks it up again.
  */
 ATTN_API int attn_bwd_noalloc(const void* Q, const void* K, const void* V,
              const void* O, const void* dO, const float* LSE, void* dQ,

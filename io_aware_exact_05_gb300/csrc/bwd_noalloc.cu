@@ -25,6 +25,10 @@
 //     stream, or synchronise in between.
 //   * The first call on each device looks up the array's device address with
 //     that device current.  Make that first call before capturing any stream.
+//     The address is cached under the id of the current CUDA context, so
+//     after cudaDeviceReset, or with another context made current on the
+//     device, the next call looks the address up again instead of using a
+//     stale one.
 //
 // The computation is the dQ-pass backward: preprocessing kernel, key-tile
 // kernel (dK, dV), query-tile kernel (dQ); bf16 results equal those of attn_bwd
@@ -47,18 +51,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 
-// Device address of the scratch array on the current device (looked up once
-// per device).  nullptr if the lookup fails.
+// Device address of the scratch array in the current context: looked up once
+// per device, and again when the device's current context is not the one the
+// cached address belongs to.  nullptr if the lookup fails.
 void* noalloc_scratch() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return nullptr;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();   // the lookup made the context current
   }
   return g_scratch_ptr[dev];
 }

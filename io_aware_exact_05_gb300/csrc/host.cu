@@ -35,7 +35,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+using PFN_ctx_get_current = CUresult (*)(CUcontext*);
+using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(p);
+  return nullptr;
+}
+
 }  // namespace
+
+unsigned long long current_context_id() {
+  static PFN_ctx_get_current get_current = nullptr;
+  static PFN_ctx_get_id get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<PFN_ctx_get_current>("cuCtxGetCurrent", 4000);
+    get_id = driver_fn<PFN_ctx_get_id>("cuCtxGetId", 12000);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;   // none yet: the runtime binds its context at its first real call
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
                     uint32_t box_x, uint32_t box_y) {
@@ -80,17 +109,22 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
   return r == CUDA_SUCCESS;
 }
 
-// Address of the status word, looked up once per device.
+// Address of the status word in the current context, looked up once per
+// device and again whenever that device's current context changes (after a
+// device reset the module is loaded again, possibly at another address).
 static int* status_word_ptr() {
   static int* ptrs[64] = {nullptr};
+  static unsigned long long ctx_ids[64] = {0};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || ctx == 0 || ctx != ctx_ids[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<int*>(p);
+    ctx_ids[dev] = current_context_id();   // the lookup made the context current
   }
   return ptrs[dev];
 }

@@ -26,6 +26,12 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, u
 
 KernelCtl default_ctl();
 
+// Unique id of the CUDA context current on this thread (the runtime's
+// primary context of the current device unless the caller made another one
+// current); 0 if it cannot be read.  Device addresses of the library's
+// file-scope __device__ arrays are cached per context under this id.
+unsigned long long current_context_id();
+
 // One block whose only wait has no arrival: records ATTN_ERR_DEVICE_TIMEOUT
 // after timeout_ns and returns (attn_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);

@@ -71,34 +71,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same, acquiring at cluster scope: for barriers that threads of the peer CTA
-// arrive on (their writes before the arrive are visible after the wait).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait.  Returns true when the phase with `parity` completed.  After
 // `timeout_ns` of polling, or as soon as another thread of the CTA raised
 // `*abort`, it records ATTN_ERR_DEVICE_TIMEOUT (first error wins) with the
 // wait site, raises `*abort` and returns false: callers then leave their loop.
-template <bool CLUSTER>
-__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volatile int* abort,
-                                            const KernelCtl& ctl, int site) {
-  auto poll = [&]() {
-    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-  };
-  if (poll()) return true;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          const KernelCtl& ctl, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t spin = 1;; ++spin) {
-    if (poll()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((spin & 255u) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > ctl.timeout_ns) {
@@ -109,51 +91,12 @@ __device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, volat
     }
   }
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          const KernelCtl& ctl, int site) {
-  return mbar_wait_t<false>(bar, parity, abort, ctl, site);
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, const KernelCtl& ctl,
-                                                  int site) {
-  return mbar_wait_t<true>(bar, parity, abort, ctl, site);
-}
 
 // Whole-warp forms (every lane waits; the result is the same on all lanes):
 // for loops that a whole warp runs, such as an MMA issuer.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
                                                const KernelCtl& ctl, int site) {
-  return __all_sync(0xffffffffu, mbar_wait_t<false>(bar, parity, abort, ctl, site));
-}
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity,
-                                                       volatile int* abort, const KernelCtl& ctl,
-                                                       int site) {
-  return __all_sync(0xffffffffu, mbar_wait_t<true>(bar, parity, abort, ctl, site));
-}
-
-// ------------------------------------------------------------ CTA clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Barrier over every thread of every CTA of the cluster (release/acquire).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
-// Shared::cluster address of the location `addr` (a shared::cta address)
-// inside the CTA of cluster rank `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Arrive (release at cluster scope) on an mbarrier given by its
-// shared::cluster address, possibly in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, ctl, site));
 }
 
 // ------------------------------------------------------------------- TMA
@@ -225,21 +168,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(NCOLS)
                : "memory");
 }
-// CTA-pair forms: executed by one warp in each CTA of the pair; every
-// tcgen05 instruction of a kernel that uses them is of the pair form.
-template <int NCOLS>
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem) {
-  static_assert(NCOLS >= 32 && NCOLS <= 512 && (NCOLS & (NCOLS - 1)) == 0, "tmem cols");
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(NCOLS)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-template <int NCOLS>
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(NCOLS)
-               : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -257,23 +185,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
-}
-
-// Pair forms: arrive on `bar` of this CTA, or on the barrier at the same
-// offset in every CTA of `mask`, once the pair MMAs issued so far are done.
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar),
-      "h"(mask)
       : "memory");
 }
 
@@ -330,9 +241,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // no other instruction lands between them.  Descriptors are passed as 32-bit
 // halves: lo[i] (start address and leading offset, which vary per MMA) and hi
 // (stride offset, version and swizzle, shared).  The first MMA accumulates
-// iff acc != 0; the other three always accumulate.  The _pair forms issue
-// the CTA-pair MMA (M = 256: A rows and B columns split between the CTAs,
-// each CTA's half at the same shared-memory and tensor-memory addresses).
+// iff acc != 0; the other three always accumulate.
 #define ATTN_MMA_SS_X4(NAME, CG, KIND)                                                           \
   __device__ __forceinline__ void NAME(uint32_t d, const uint32_t(&alo)[4], uint32_t ahi,       \
                                        const uint32_t(&blo)[4], uint32_t bhi, uint32_t idesc,   \
@@ -354,7 +263,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");                                                                            \
   }
 ATTN_MMA_SS_X4(mma_ss_x4, "1", "f16")
-ATTN_MMA_SS_X4(mma_pair_ss_x4, "2", "f16")
 ATTN_MMA_SS_X4(mma_ss_x4_f8, "1", "f8f6f4")   // e4m3 operands: 32 per MMA along K
 #undef ATTN_MMA_SS_X4
 
@@ -379,7 +287,6 @@ ATTN_MMA_SS_X4(mma_ss_x4_f8, "1", "f8f6f4")   // e4m3 operands: 32 per MMA along
         : "memory");                                                                            \
   }
 ATTN_MMA_TS_X4(mma_ts_x4, "1", "f16")
-ATTN_MMA_TS_X4(mma_pair_ts_x4, "2", "f16")
 // e4m3 A from tensor memory: four values per 32-bit column, so the eight
 // columns per MMA again hold its 32 values of K
 ATTN_MMA_TS_X4(mma_ts_x4_f8, "1", "f8f6f4")
