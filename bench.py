@@ -490,7 +490,7 @@ def run_ours(args, w):
           for n in ("o", "lse", "dq", "dk", "dv")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(E2E_MIN_STEPS, args.steps)
+    e2e_steps = args.e2e_steps or max(E2E_MIN_STEPS, args.steps)
     buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
     e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
@@ -649,7 +649,7 @@ def run_fp8(args, w):
           for n in ("o", "lse")}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    e2e_steps = max(E2E_MIN_STEPS, args.steps)
+    e2e_steps = args.e2e_steps or max(E2E_MIN_STEPS, args.steps)
     buf1 = {n: torch.empty_like(t) for n, t in buf0.items()}
     e2e_ms_pipelined(step, [buf0, buf1], hx, ho, 2, st)     # warm-up
     if dist:
@@ -715,6 +715,9 @@ def main():
                     help="dQ mode; auto: atomic for d <= 128, the dQ pass above")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end leg (default: max(%d, --steps))"
+                         % E2E_MIN_STEPS)
     ap.add_argument("--sustain-s", type=float, default=3.0,
                     help="seconds of back-to-back steps after the timed region, reported "
                          "against the sustained peak (0: skip)")

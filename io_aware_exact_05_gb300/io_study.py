@@ -49,13 +49,13 @@ __all__ = ["main"]
 B, H = 1, 4
 
 
-def _run(path, n, d, b=B, h=H, causal=False):
+def _run(path, n, d, b=B, h=H, causal=False, dtype="bf16"):
     import torch
 
     from . import attn
     from .inputs import Workload, make_inputs
 
-    w = Workload("io", b, h, n, d, "bf16", causal, 1.0, 2000 + n + d)
+    w = Workload("io", b, h, n, d, dtype, causal, 1.0, 2000 + n + d)
     x = make_inputs(w)
     dev = torch.device("cuda", 0)
     q, k, v, do = (x[t].to(dev) for t in ("q", "k", "v", "do"))
@@ -170,13 +170,15 @@ def main(argv=None):
     r.add_argument("--B", type=int, default=B)
     r.add_argument("--H", type=int, default=H)
     r.add_argument("--causal", action="store_true")
+    r.add_argument("--dtype", choices=["bf16", "f32"], default="bf16",
+                   help="f32 runs the fp32 SIMT kernels (fused path only)")
     s = sub.add_parser("summarize")
     s.add_argument("csv", nargs="+")
     kk = sub.add_parser("kernels")
     kk.add_argument("csv")
     a = ap.parse_args(argv)
     if a.cmd == "run":
-        _run(a.path, a.n, a.d, a.B, a.H, a.causal)
+        _run(a.path, a.n, a.d, a.B, a.H, a.causal, a.dtype)
     elif a.cmd == "kernels":
         _kernels(a.csv)
     else:
