@@ -264,6 +264,28 @@ ATTN_API int attn_bwd_dq(const void* Q, const void* K, const void* V,
              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_dkdv_keys -- attn_bwd_dkdv with key tiles of key_rows keys (128,
+ * 64 or 32; ATTN_ERR_INVALID_ARG otherwise), for measuring how the
+ * backward's memory traffic depends on the on-chip memory it works with
+ * ("On the fine-grained I/O complexity of attention backward passes",
+ * Theorem 1.1: with a cache of M words the tiled backward moves
+ * Theta((n^2 d^2 + n d^3) / M) words).  A CTA keeps the K and V rows of its
+ * key tile on chip and streams every Q and dO tile past them, so halving
+ * key_rows doubles that stream (and the dQ shares added per key tile).  Each
+ * CTA still runs the 128-key tile computation but owns only its first
+ * key_rows keys (the other keys' probabilities are set to 0), so smaller
+ * tiles are also slower; key_rows = 128 is attn_bwd_dkdv.  Results equal
+ * attn_bwd_dkdv's up to the order of the dQ additions.  Same arguments and
+ * workspace as attn_bwd_dkdv; bf16, one key/value head per query head; d = 64
+ * and 128 in ATTN_DQ_ATOMIC (or AUTO) mode only (ATTN_ERR_UNSUPPORTED for
+ * ATTN_DQ_PASS), d = 256 in pass mode.
+ */
+ATTN_API int attn_bwd_dkdv_keys(const void* Q, const void* K, const void* V,
+             const void* dO, void* dK, void* dV, int B, int H, int n, int d,
+             attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
+             int key_rows, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_noalloc -- the backward pass for callers that cannot allocate.
  * The pages have no counterpart to this entry point; it is a deployment aid.
  * Some callers cannot pass a workspace: they hold no device allocator of

@@ -16,7 +16,7 @@ __all__ = [
     "ATTN_BF16", "ATTN_F32", "ATTN_DQ_AUTO", "ATTN_DQ_ATOMIC", "ATTN_DQ_PASS",
     "AttnError", "lib", "lib_path",
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
-    "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
+    "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_bwd_dkdv_keys",
     "attn_fwd_gqa", "attn_bwd_gqa", "attn_bwd_gqa_workspace_size",
     "attn_fwd_sparse", "attn_bwd_sparse", "attn_fwd_sparse_workspace_size", "attn_fwd_fp8",
     "forward_fp8", "attn_quantize_fp8", "attn_quantize_fp8_workspace_size", "quantize_fp8",
@@ -91,6 +91,8 @@ def lib():
             L.attn_bwd_dkdv.restype = i
             L.attn_bwd_dq.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
             L.attn_bwd_dq.restype = i
+            L.attn_bwd_dkdv_keys.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, i, vp, sz, vp]
+            L.attn_bwd_dkdv_keys.restype = i
             L.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
             L.attn_bwd_noalloc.restype = i
             L.attn_mat_workspace_size.argtypes = [i, i, i, i]
@@ -349,6 +351,18 @@ def attn_bwd_dkdv(Q, K, V, dO, dK, dV, scale, causal, mode, workspace, stream=No
                              _dtype_code(Q), float(scale), int(bool(causal)), int(mode), wp, wb,
                              _stream(stream))
     _check(rc, "attn_bwd_dkdv")
+
+
+def attn_bwd_dkdv_keys(Q, K, V, dO, dK, dV, scale, causal, mode, key_rows, workspace,
+                       stream=None):
+    """attn_bwd_dkdv with key tiles of key_rows keys (128, 64, 32): the IO
+    study's way of changing the on-chip memory of the key-tile kernel."""
+    B, H, n, d = _shape(Q)
+    wp, wb = _ws(workspace)
+    rc = lib().attn_bwd_dkdv_keys(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dK), _ptr(dV), B, H,
+                                  n, d, _dtype_code(Q), float(scale), int(bool(causal)),
+                                  int(mode), int(key_rows), wp, wb, _stream(stream))
+    _check(rc, "attn_bwd_dkdv_keys")
 
 
 def attn_bwd_dq(Q, K, V, dO, dQ, scale, causal, mode, workspace, stream=None):

@@ -368,6 +368,23 @@ int attn_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, v
                        workspace_bytes, stream);
 }
 
+int attn_bwd_dkdv_keys(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                       void* dV, int B, int H, int n, int d, attn_dtype dtype, float scale,
+                       int causal, attn_dq_mode mode, int key_rows, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (key_rows != 32 && key_rows != 64 && key_rows != 128) return ATTN_ERR_INVALID_ARG;
+  if (!ptrs_ok({Q, K, V, dO, dK, dV})) return ATTN_ERR_INVALID_ARG;
+  attn_dq_mode m;
+  BwdWorkspace w;
+  int rc = bwd_setup(B, H, H, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m, &w);
+  if (rc) return rc;
+  if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (d <= 128 && m != ATTN_DQ_ATOMIC) return ATTN_ERR_UNSUPPORTED;
+  return launch_bwd_kv_study(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr,
+                             dK, dV, B * H, key_rows, n, (int)round_up(n, 128), d, scale, causal,
+                             default_ctl(), static_cast<cudaStream_t>(stream));
+}
+
 int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
                 int H, int n, int d, attn_dtype dtype, float scale, int causal, attn_dq_mode mode,
                 void* workspace, size_t workspace_bytes, void* stream) {

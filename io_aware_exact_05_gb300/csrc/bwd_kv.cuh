@@ -91,7 +91,11 @@ enum : int { B_KV = 0, B_QF = 1, B_QE = 3, B_SF = 5, B_DPF = 6, B_PR = 7, B_DVD 
 // one-head-per-head kernel keeps its simple loops).  SPARSE: a block pattern
 // keeps only some query tiles for this key tile; the CTA walks that list
 // (every listed tile lies in kept blocks) instead of the dense range.
-template <int DH, bool DQ, bool GROUPED, bool SPARSE>
+// KR < 128 (IO study only): the CTA owns the first KR keys of its 128-key
+// tile, key tiles start KR keys apart, and the other keys' probabilities are
+// set to 0, so the CTA keeps KR keys' worth of K and V on chip and Q and dO
+// are streamed 128 / KR times as often.
+template <int DH, bool DQ, bool GROUPED, bool SPARSE, int KR = 128>
 __global__ void __launch_bounds__(DQ ? 512 : 384, 1)
 bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -102,6 +106,8 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                   int n_pad, float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = KvCfgT<DH>;
   constexpr int D = DH;
+  static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED),
+                "owned key rows: a dense, one-head-per-head study instance");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -124,7 +130,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int nkvh = (heads_fast ? (int)gridDim.x : (int)gridDim.y) / gsplit;
   const int bh = hx % nkvh;           // key/value head (K, V, dK, dV)
   const int part = hx / nkvh;         // part of the group
-  const int k0 = kt * C::BNK;
+  const int k0 = kt * KR;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
   const int* qlist = SPARSE ? tl.lists + (size_t)kt * tl.stride : nullptr;
@@ -379,6 +385,12 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
           }
         }
+        if constexpr (KR < C::BNK) {   // keys of the next study tile: no contribution
+          if (r >= KR) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) p[c] = 0.f;
+          }
+        }
 #pragma unroll
         for (int c0 = 0; c0 < NC; c0 += 32) {
           uint32_t pk[16];
@@ -458,7 +470,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (key < n) {
+        if (key < n && (KR == C::BNK || r < KR)) {
           if (acc) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
@@ -532,7 +544,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 2) tmem_dealloc<512>(tmem);
 }
 
-template <int DH, bool DQ, bool GROUPED, bool SPARSE>
+template <int DH, bool DQ, bool GROUPED, bool SPARSE, int KR = 128>
 int launch_kv(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
              const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
              int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
@@ -550,11 +562,11 @@ int launch_kv(const void* Q, const void* K, const void* V, const void* dO, const
   } else {
     tdq = tq;   // not read
   }
-  auto kern = bwd_kv128_kernel<DH, DQ, GROUPED, SPARSE>;
+  auto kern = bwd_kv128_kernel<DH, DQ, GROUPED, SPARSE, KR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
-  const int nkt = ceil_div(n, C::BNK);
+  const int nkt = ceil_div(n, KR);
   dim3 grid = (causal || SPARSE) ? dim3(BHkv * gsplit, nkt) : dim3(nkt, BHkv * gsplit);
   kern<<<grid, DQ ? 512 : 384, C::SMEM, st>>>(tq, tk, tv, tg, tdq, LSE2, Dv, dQacc,
                                               static_cast<__nv_bfloat16*>(dK),

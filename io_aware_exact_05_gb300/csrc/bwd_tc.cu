@@ -107,7 +107,11 @@ enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR 
 // GROUPED: query heads share key/value heads (compiled separately so that the
 // one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
 // the listed query tiles of a block pattern instead of the dense range.
-template <int D, bool DQ, bool GROUPED, bool SPARSE>
+// KR < 128 (IO study only): the CTA owns the first KR keys of its 128-key
+// tile, key tiles start KR keys apart, and the other keys' probabilities are
+// set to 0 (less K and V kept on chip, Q and dO streamed 128 / KR times as
+// often).
+template <int D, bool DQ, bool GROUPED, bool SPARSE, int KR = 128>
 __global__ void __launch_bounds__(KvCfg<D, DQ>::NTHREADS, 1)
 bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -117,6 +121,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n, int n_pad,
               float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = KvCfg<D, DQ>;
+  static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED && !DQ),
+                "owned key rows: a dense, one-head-per-head study instance");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -140,7 +146,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int part = (int)blockIdx.z;              // part of the group (gsplit > 1)
   const bool want_dv = !C::SPLIT_OUT || oh == 0;
   const bool want_dk = !C::SPLIT_OUT || oh == 1;
-  const int k0 = kt * C::BNK;
+  const int k0 = kt * KR;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
   const int* qlist = SPARSE ? tl.lists + (size_t)kt * tl.stride : nullptr;
@@ -362,6 +368,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             p[c0 + i] = v;
           }
         }
+        if constexpr (KR < C::BNK) {   // keys of the next study tile: no contribution
+          if (r >= KR) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) p[c] = 0.f;
+          }
+        }
         if (want_dv) {   // P^T in bf16 over S^T: the A operand of dV
 #pragma unroll
           for (int c0 = 0; c0 < NC; c0 += 32) {
@@ -442,7 +454,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (key < n) {
+        if (key < n && (KR == C::BNK || r < KR)) {
           if (acc) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
@@ -766,7 +778,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   if (warp == 2) tmem_dealloc<512>(tmem);
 }
 
-template <int D, bool DQ>
+template <int D, bool DQ, int KR = 128>
 int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
                   const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
                   int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
@@ -780,12 +792,16 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
       !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   if (tl.lists && hm.group > 1) return ATTN_ERR_UNSUPPORTED;
-  auto kern = tl.lists        ? bwd_kv_kernel<D, DQ, false, true>
-              : hm.group > 1 ? bwd_kv_kernel<D, DQ, true, false>
-                             : bwd_kv_kernel<D, DQ, false, false>;
+  auto kern = bwd_kv_kernel<D, DQ, false, false, KR>;
+  if constexpr (KR == C::BNK) {
+    if (tl.lists) kern = bwd_kv_kernel<D, DQ, false, true>;
+    else if (hm.group > 1) kern = bwd_kv_kernel<D, DQ, true, false>;
+  } else if (tl.lists || hm.group > 1) {
+    return ATTN_ERR_UNSUPPORTED;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const int nkt = ceil_div(n, C::BNK);
+  const int nkt = ceil_div(n, KR);
   dim3 grid = (causal || tl.lists) ? dim3(BHkv * C::NOUT, nkt, gsplit)
                                    : dim3(nkt, BHkv * C::NOUT, gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
@@ -845,6 +861,27 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
     default: return ATTN_ERR_UNSUPPORTED;
   }
 #undef ATTN_KV
+}
+
+int launch_bwd_kv_study(const void* Q, const void* K, const void* V, const void* dO,
+                        const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                        int BH, int key_rows, int n, int n_pad, int d, float scale, int causal,
+                        const KernelCtl& ctl, cudaStream_t st) {
+  const HeadMap hm{BH, 1};
+  if (d != 256)
+    return launch_bwd_kv_study_d64_128(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, BH, key_rows, n,
+                                       n_pad, d, scale, causal, ctl, st);
+  if (dQacc) return ATTN_ERR_UNSUPPORTED;
+#define ATTN_KVS(KRR)                                                                          \
+  return launch_kv_cfg<256, false, KRR>(Q, K, V, dO, LSE2, Dv, nullptr, dK, dV, nullptr, nullptr, \
+                                        BH, hm, 1, TileLists(), n, n_pad, scale, causal, ctl, st)
+  switch (key_rows) {
+    case 128: ATTN_KVS(128);
+    case 64: ATTN_KVS(64);
+    case 32: ATTN_KVS(32);
+    default: return ATTN_ERR_INVALID_ARG;
+  }
+#undef ATTN_KVS
 }
 
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,

@@ -114,6 +114,19 @@ int launch_bwd_kv128_tc(const void* Q, const void* K, const void* V, const void*
                         float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
                         const TileLists& tl, int n, int n_pad, float scale, int causal,
                         const KernelCtl& ctl, cudaStream_t st);
+// The key-tile backward with key tiles of key_rows keys (128, 64 or 32), for
+// measuring how its memory traffic depends on the keys a CTA keeps on chip:
+// each CTA still computes a 128-key tile but owns only its first key_rows
+// keys.  Dense, one key/value head per query head.  d = 64 and 128 add dQ
+// shares into dQacc (required); d = 256 takes none (dQacc must be null).
+int launch_bwd_kv_study(const void* Q, const void* K, const void* V, const void* dO,
+                        const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
+                        int BH, int key_rows, int n, int n_pad, int d, float scale, int causal,
+                        const KernelCtl& ctl, cudaStream_t st);
+int launch_bwd_kv_study_d64_128(const void* Q, const void* K, const void* V, const void* dO,
+                                const float* LSE2, const float* Dv, float* dQacc, void* dK,
+                                void* dV, int BH, int key_rows, int n, int n_pad, int d,
+                                float scale, int causal, const KernelCtl& ctl, cudaStream_t st);
 // Query-tile backward: dQ with no atomics.
 int launch_bwd_q_tc(const void* Q, const void* K, const void* V, const void* dO,
                     const float* LSE2, const float* Dv, void* dQ, int BH, const HeadMap& hm,

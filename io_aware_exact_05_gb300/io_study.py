@@ -30,6 +30,28 @@ after its three forward launches) and prints bytes per path with reference
 counts: the compulsory bytes and n^2 d^2 / M with M the K, V tile a CTA keeps
 on chip.
 
+Tile-size axis (the theorem's M at fixed n and d): `run --key-rows R` runs
+the fused backward with key tiles of R = 128, 64 or 32 keys
+(attn_bwd_dkdv_keys: a CTA keeps R keys' K and V rows on chip and streams
+every Q and dO tile past them), captured on the key-tile kernel alone:
+
+    ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,lts__t_bytes.sum \
+        --clock-control none -k regex:bwd_kv --csv --log-file io_keys_n4096_d128_r64.csv \
+        python -m io_aware_exact_05_gb300.io_study run --path fused --n 4096 --d 128 --key-rows 64
+    python -m io_aware_exact_05_gb300.io_study keyrows io_keys_*.csv
+
+`keyrows` prints, per (n, d, R), the kernel's bytes against n^2 d^2 / M with
+M = 2 R d (the K and V rows the CTA keeps).
+
+Sparse attention ("On the fine-grained I/O complexity of attention backward
+passes", Theorem 4.5: Omega(min{Z_in^2 / M, Z_in sqrt(Z_QK) / sqrt(M)}) with
+Z_in nonzero input entries and Z_QK kept score entries, split at
+M = Z_in^2 / Z_QK): `run --path sparse --pattern W,G,R` runs the
+block-sparse forward and backward over make_block_mask(n, W, G, R) (seed
+3000 + n); capture the key-tile kernel and summarise with `sparse`, which
+recomputes Z_QK from the same pattern and takes Z_in = n d (the inputs are
+dense; with Z_QK = n^2 both terms become Theorem 1.1's).
+
 `kernels` reads a launch list taken with
 `ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum`
 and prints, per launch, its time, DRAM bytes and DRAM GB/s against the
@@ -49,7 +71,15 @@ __all__ = ["main"]
 B, H = 1, 4
 
 
-def _run(path, n, d, b=B, h=H, causal=False, dtype="bf16"):
+def sparse_pattern(n, pattern):
+    """The block pattern of a sparse IO-study run (uint8 [nb][nb])."""
+    from .inputs import make_block_mask
+
+    w_, g_, r_ = pattern
+    return make_block_mask(n, w_, g_, r_, 3000 + n)
+
+
+def _run(path, n, d, b=B, h=H, causal=False, dtype="bf16", key_rows=0, pattern=None):
     import torch
 
     from . import attn
@@ -59,7 +89,20 @@ def _run(path, n, d, b=B, h=H, causal=False, dtype="bf16"):
     x = make_inputs(w)
     dev = torch.device("cuda", 0)
     q, k, v, do = (x[t].to(dev) for t in ("q", "k", "v", "do"))
-    if path == "fused":   # tiled forward, then the tiled backward (key-tile kernel + dQ)
+    if path == "sparse":   # block-sparse forward and backward
+        bm = sparse_pattern(n, pattern).to(dev)
+        o, lse = attn.forward(q, k, v, causal=causal, block_mask=bm)
+        attn.backward(q, k, v, o, do, lse, causal=causal, block_mask=bm)
+    elif path == "fused" and key_rows:   # the backward's stages with R-key tiles
+        o, lse = attn.forward(q, k, v, causal=causal)
+        mode = attn.ATTN_DQ_PASS if d == 256 else attn.ATTN_DQ_ATOMIC
+        ws = torch.empty(attn.attn_bwd_workspace_size(b, h, n, d, attn.ATTN_BF16, causal, mode),
+                         dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        attn.attn_bwd_preprocess(o, do, lse, causal, mode, ws)
+        attn.attn_bwd_dkdv_keys(q, k, v, do, dk, dv, w.scale, causal, mode, key_rows, ws)
+        attn.attn_bwd_dq(q, k, v, do, dq, w.scale, causal, mode, ws)
+    elif path == "fused":   # tiled forward, then the tiled backward (key-tile kernel + dQ)
         o, lse = attn.forward(q, k, v, causal=causal)
         attn.backward(q, k, v, o, do, lse, causal=causal)
     else:                 # materialise-P: S, P, dP, dS as n x n matrices in HBM
@@ -138,6 +181,65 @@ def _summarize(paths):
             r["fused_l2"] / r["n2d2_over_m"]))
 
 
+def _keyrows(paths):
+    """Key-tile kernel bytes per (n, d, R) from captures of that kernel alone."""
+    out = []
+    for p in paths:
+        m = re.search(r"n(\d+)_d(\d+)_r(\d+)", p)
+        n, d, r = (int(x) for x in m.groups())
+        ls = [l for l in _rows(p) if l["name"].startswith("bwd_kv")]
+        dram = sum(l.get("dram__bytes_read.sum", 0.0) + l.get("dram__bytes_write.sum", 0.0)
+                   for l in ls)
+        l2 = sum(l.get("lts__t_bytes.sum", 0.0) for l in ls)
+        m_elems = 2 * r * d                       # K and V rows the CTA keeps
+        ref = B * H * n * n * d * d / m_elems * 2  # n^2 d^2 / M words, in bf16 bytes
+        out.append({"n": n, "d": d, "r": r, "M": m_elems, "dram": dram, "l2": l2, "ref": ref})
+    out.sort(key=lambda x: (x["d"], x["n"], -x["r"]))
+    base = {(x["n"], x["d"]): x["l2"] for x in out if x["r"] == 128}
+    print("| n | d | key rows R | M = 2 R d | key-tile kernel L2<->SM MB | x vs R = 128 | "
+          "DRAM MB | n^2 d^2 / M MB | L2 / (n^2 d^2 / M) |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for x in out:
+        b0 = base.get((x["n"], x["d"]))
+        print("| %d | %d | %d | %d | %.1f | %s | %.1f | %.1f | %.2f |" % (
+            x["n"], x["d"], x["r"], x["M"], x["l2"] / 1e6,
+            "%.2f" % (x["l2"] / b0) if b0 else "-", x["dram"] / 1e6, x["ref"] / 1e6,
+            x["l2"] / x["ref"]))
+
+
+def _sparse(paths):
+    """Key-tile kernel bytes of the block-sparse backward against Theorem 4.5."""
+    from .flops import kept_entries
+
+    out = []
+    for p in paths:
+        m = re.search(r"n(\d+)_d(\d+)_w(\d+)g(\d+)r(\d+)", p)
+        n, d, w_, g_, r_ = (int(x) for x in m.groups())
+        mask = sparse_pattern(n, (w_, g_, r_)).numpy()
+        z_qk = kept_entries(mask, n, False)
+        ls = [l for l in _rows(p) if l["name"].startswith("bwd_kv")]
+        dram = sum(l.get("dram__bytes_read.sum", 0.0) + l.get("dram__bytes_write.sum", 0.0)
+                   for l in ls)
+        l2 = sum(l.get("lts__t_bytes.sum", 0.0) for l in ls)
+        z_in = n * d
+        m_el = 256 * d                               # K and V tiles of a key-tile CTA
+        out.append({"n": n, "d": d, "pat": (w_, g_, r_), "frac": mask.mean(), "zqk": z_qk,
+                    "l2": l2, "dram": dram, "t1": z_in * z_in / m_el,
+                    "t2": z_in * z_qk ** 0.5 / m_el ** 0.5, "split": z_in * z_in / z_qk,
+                    "m": m_el})
+    out.sort(key=lambda x: (x["d"], x["n"], x["zqk"]))
+    print("| n | d | pattern (window, global, random) | blocks kept | Z_QK / n^2 | key-tile "
+          "kernel L2<->SM MB (per head) | L2 bytes per kept entry | DRAM MB (per head) | "
+          "Z_in^2/M MB | Z_in sqrt(Z_QK)/sqrt(M) MB | M = 256 d | split Z_in^2/Z_QK | regime |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|---|---|")
+    for x in out:
+        regime = "large cache" if x["m"] >= x["split"] else "small cache"
+        print("| %d | %d | %s | %.1f %% | %.4f | %.1f | %.2f | %.2f | %.2f | %.2f | %d | %.0f | %s |"
+              % (x["n"], x["d"], "%d, %d, %d" % x["pat"], 100 * x["frac"], x["zqk"] / x["n"] ** 2,
+                 x["l2"] / H / 1e6, x["l2"] / H / x["zqk"], x["dram"] / H / 1e6,
+                 2 * x["t1"] / 1e6, 2 * x["t2"] / 1e6, x["m"], x["split"], regime))
+
+
 def _hbm_peak():
     p = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                      "MEASURED_PEAKS.json")
@@ -164,7 +266,9 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     sub = ap.add_subparsers(dest="cmd", required=True)
     r = sub.add_parser("run")
-    r.add_argument("--path", choices=["fused", "mat"], required=True)
+    r.add_argument("--path", choices=["fused", "mat", "sparse"], required=True)
+    r.add_argument("--pattern", default="2,1,2",
+                   help="sparse: window, global and random blocks of the block pattern")
     r.add_argument("--n", type=int, required=True)
     r.add_argument("--d", type=int, required=True)
     r.add_argument("--B", type=int, default=B)
@@ -172,13 +276,25 @@ def main(argv=None):
     r.add_argument("--causal", action="store_true")
     r.add_argument("--dtype", choices=["bf16", "f32"], default="bf16",
                    help="f32 runs the fp32 SIMT kernels (fused path only)")
+    r.add_argument("--key-rows", type=int, default=0, choices=[0, 32, 64, 128],
+                   help="fused bf16 backward with key tiles of this many keys (0: the product "
+                        "kernels through attn_bwd)")
+    kr = sub.add_parser("keyrows")
+    kr.add_argument("csv", nargs="+")
+    sp = sub.add_parser("sparse")
+    sp.add_argument("csv", nargs="+")
     s = sub.add_parser("summarize")
     s.add_argument("csv", nargs="+")
     kk = sub.add_parser("kernels")
     kk.add_argument("csv")
     a = ap.parse_args(argv)
     if a.cmd == "run":
-        _run(a.path, a.n, a.d, a.B, a.H, a.causal, a.dtype)
+        _run(a.path, a.n, a.d, a.B, a.H, a.causal, a.dtype, a.key_rows,
+             tuple(int(x) for x in a.pattern.split(",")))
+    elif a.cmd == "keyrows":
+        _keyrows(a.csv)
+    elif a.cmd == "sparse":
+        _sparse(a.csv)
     elif a.cmd == "kernels":
         _kernels(a.csv)
     else:

@@ -156,6 +156,27 @@ def test_backward_stage_argument_checks(L):
     assert L.attn_launch_count() == before
 
 
+def test_key_rows_study_argument_checks(L):
+    """attn_bwd_dkdv_keys checks like attn_bwd_dkdv, plus the key tile size
+    and the dQ mode its instances exist for; nothing is launched."""
+    ws = ctypes.c_void_p(1 << 24)
+    before = L.attn_launch_count()
+
+    def kv(*, d=128, dt=0, mode=0, rows=64, wsb=1 << 30, ptr=FAKE):
+        return L.attn_bwd_dkdv_keys(ptr, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, d, dt, 0.1, 0,
+                                    mode, rows, ws, wsb, None)
+
+    for rows in (0, 16, 48, 96, 256):
+        assert kv(rows=rows) == 1
+    assert kv(ptr=ctypes.c_void_p(0)) == 1
+    assert kv(dt=1) == 1                                   # bf16 only
+    assert kv(d=96) == 2
+    assert kv(mode=2) == 2 and kv(d=64, mode=2) == 2       # d <= 128: atomic dQ only
+    assert kv(d=256, mode=1) == 2                          # d = 256: the dQ pass only
+    assert kv(wsb=16) == 3
+    assert L.attn_launch_count() == before
+
+
 def test_gqa_argument_checks(L):
     def fwd(H=4, Hkv=2, d=64):
         return L.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, H, Hkv, 128, d, 0, 0.125, 0, None)
