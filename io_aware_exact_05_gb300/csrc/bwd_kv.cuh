@@ -74,10 +74,18 @@ struct KvCfgT {
   static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024 + (DS_OVER_DO ? 0 : DS_BYTES);
   static constexpr uint32_t K_OFF = 0, V_OFF = KV_BYTES;
   static constexpr uint32_t ST_OFF = 2 * KV_BYTES;
-  static constexpr uint32_t QS_OFF = ST_OFF + STG * STAGE;     // dQ staging: 2 x [64][32] fp32
-  static constexpr uint32_t QS_BYTES = BM * 32 * 4;             // 16 KB, 128-byte swizzle
+  // dQ staging: per 64-row half of the tile, QS_NBUF boxes of [64][32] fp32
+  // (8 KB each, 128-byte swizzle), so each half keeps QS_NBUF reduce-adds
+  // in flight
+  static constexpr int QS_NBUF = 2;
+  static constexpr uint32_t QS_BOX = 64 * 32 * 4;
+  static constexpr uint32_t QS_OFF = ST_OFF + STG * STAGE;
+  static constexpr uint32_t QS_BYTES = 2 * QS_NBUF * QS_BOX;
   static constexpr uint32_t BAR_OFF = QS_OFF + QS_BYTES;
-  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  // 1 KB of slack to align the base when it fits; otherwise the kernel checks
+  // that the dynamic shared memory starts 1024-byte aligned
+  static constexpr uint32_t ALIGN_SLACK = (BAR_OFF + 256 + 1024 <= 232448) ? 1024 : 0;
+  static constexpr uint32_t SMEM = BAR_OFF + 256 + ALIGN_SLACK;
   static constexpr int DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -109,6 +117,14 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED),
                 "owned key rows: a dense, one-head-per-head study instance");
   extern __shared__ uint8_t smem_raw[];
+  if constexpr (C::ALIGN_SLACK == 0) {
+    // no room to align the layout: it needs the base 1024-byte aligned (the
+    // 128-byte swizzle atoms); report and leave before touching anything
+    if (smem_u32(smem_raw) & 1023u) {
+      if (threadIdx.x == 0) record_error(ctl, ATTN_ERR_CUDA, SITE_BWD_SMEM_ALIGN);
+      return;
+    }
+  }
   uint8_t* smem = align_1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + C::BAR_OFF;
@@ -488,16 +504,18 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // Pulls the whole 128 x D fp32 dQ tile out of TMEM (thread = query row)
     // and releases the columns at once.  Each half (warps 2h, 2h+1 of the
     // group: rows [64h, 64h+64)) then adds its rows into the accumulator as
-    // D / 32 boxes of 64 x 32 through its own staging buffer, with its own named
-    // barrier and bulk group, so the two halves keep two reduce-adds in
-    // flight.  Rows past n are clipped by the tensor map.
+    // D / 32 boxes of 64 x 32 through its own ring of QS_NBUF staging boxes,
+    // with its own named barrier and bulk group, so each half keeps QS_NBUF
+    // reduce-adds in flight.  Rows past n are clipped by the tensor map; a
+    // half that lies wholly past n adds nothing.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int half = q >> 1, hr = r - 64 * half;
     const bool lead = (lane == 0) && (q & 1) == 0;
     const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::DP_COL;
-    uint8_t* stage = smem + C::QS_OFF + half * (C::QS_BYTES / 2);
+    uint8_t* ring = smem + C::QS_OFF + half * (C::QS_NBUF * C::QS_BOX);
+    int slot = 0;
     bool go = true;
     for (int gi = 0, u = 0; go && gi < gper; ++gi) {
       const int bq = qbase + gi;
@@ -515,9 +533,12 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_fence_before();
         mbar_arrive(bar(B_DQE));        // the dP^T columns may be refilled now
         const int row0 = qtile(ut) * C::BM + 64 * half;
+        if (row0 >= n) continue;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          if (lead) bulk_wait_read_all();
+          uint8_t* stage = ring + slot * C::QS_BOX;
+          slot = (slot + 1 == C::QS_NBUF) ? 0 : slot + 1;
+          if (lead) bulk_wait_read<C::QS_NBUF - 1>();   // this box's last reduce-add has read it
           named_bar_sync(1 + half, 64);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -526,7 +547,7 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                             scale * __uint_as_float(v[c][4 * j + 2]), scale * __uint_as_float(v[c][4 * j + 3]));
           fence_proxy_async_smem();
           named_bar_sync(1 + half, 64);
-          if (lead && row0 < n) {
+          if (lead) {
             tma_reduce_add_3d(&tmdQ, smem_u32(stage), 32 * c, row0, bq);
             bulk_commit_group();
           }
