@@ -139,10 +139,29 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
   // head's K and V shared in L2 by CTAs that run together.  The parts of a
   // split group count as heads here (hx = part * key/value heads + head), so
-  // the last part's long tiles do not trail either.
+  // the last part's long tiles do not trail either.  Causal and dense, the
+  // heads go in groups of kHeadGroup (the last group may be smaller), each
+  // group in that order, group after group: only one group's Q, dO and dQ
+  // accumulators are then in flight, which keeps them in L2 (DRAM bytes per
+  // launch 2.92 -> 0.64 GB on B2 H16 n8192 d128, at the same speed) while
+  // every long tile still starts before the short ones of its group.
   const bool heads_fast = causal || SPARSE;
-  const int kt = heads_fast ? blockIdx.y : blockIdx.x;
-  const int hx = heads_fast ? blockIdx.x : blockIdx.y;
+  int kt = heads_fast ? blockIdx.y : blockIdx.x;
+  int hx = heads_fast ? blockIdx.x : blockIdx.y;
+  if (causal && !SPARSE) {
+    constexpr int kHeadGroup = 8;
+    const int nh = (int)gridDim.x, ntile = (int)gridDim.y;
+    const int L = (int)(blockIdx.x + gridDim.x * blockIdx.y);
+    const int full = nh / kHeadGroup, per = kHeadGroup * ntile;
+    if (L < full * per) {
+      kt = (L % per) / kHeadGroup;
+      hx = (L / per) * kHeadGroup + (L % per) % kHeadGroup;
+    } else {
+      const int rest = nh - full * kHeadGroup, Lr = L - full * per;
+      kt = Lr / rest;
+      hx = full * kHeadGroup + Lr % rest;
+    }
+  }
   const int nkvh = (heads_fast ? (int)gridDim.x : (int)gridDim.y) / gsplit;
   const int bh = hx % nkvh;           // key/value head (K, V, dK, dV)
   const int part = hx / nkvh;         // part of the group
