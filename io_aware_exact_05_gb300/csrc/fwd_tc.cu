@@ -56,7 +56,13 @@ struct FwdCfg {
   static constexpr bool Q_IN_TMEM = (D == 256 && QT == 1);
   static constexpr int Q_COL = 2 * BN + QT * D;
   static constexpr int NTHREADS = 128 * (1 + QT);
-  static_assert(2 * BN + QT * D + (Q_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
+  static constexpr int TMEM_NEED = 2 * BN + QT * D + (Q_IN_TMEM ? D / 2 : 0);
+  // allocation: a power of two of at least 32 columns; at most 256 columns
+  // and half the shared memory let two CTAs share an SM (each with its own
+  // producer, MMA issuer and softmax warpgroup)
+  static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int MINB = (TMEM_COLS <= 256 && SMEM <= 232448 / 2) ? 2 : 1;
+  static_assert(TMEM_NEED <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -108,7 +114,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // union over its query tiles, each entry flagging the tiles it is kept for)
 // instead of the dense range.
 template <int D, int BN, int QT, bool GROUPED, bool SPARSE>
-__global__ void __launch_bounds__(FwdCfg<D, BN, QT>::NTHREADS, 1)
+__global__ void __launch_bounds__(FwdCfg<D, BN, QT>::NTHREADS, FwdCfg<D, BN, QT>::MINB)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
               float* __restrict__ LSE, HeadMap hm, TileLists tl, int n, float scale_log2,
@@ -179,7 +185,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 2) tmem_alloc<512>(smem_u32(tmem_slot));
+  if (warp == 2) tmem_alloc<C::TMEM_COLS>(smem_u32(tmem_slot));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -490,7 +496,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc<512>(tmem);
+  if (warp == 2) tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
 template <int D, int BN, int QT>
@@ -521,17 +527,20 @@ int launch_cfg(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 }  // namespace
 
+// d = 64: one 128-query tile and 64-key tiles per CTA (192 TMEM columns,
+// 66 KB of shared memory), so two CTAs share an SM; d = 128: two query tiles
+// that ping-pong on one MMA issuer; d = 256: one query tile, Q in TMEM.
 void fwd_tiling(int d, int* query_rows, int* query_tiles, int* kv_rows) {
   *query_rows = 128;
-  *query_tiles = d == 256 ? 1 : 2;
-  *kv_rows = d == 256 ? 64 : 128;
+  *query_tiles = d == 128 ? 2 : 1;
+  *kv_rows = d == 128 ? 128 : 64;
 }
 
 int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
                   const HeadMap& hm, const TileLists& tl, int n, int d, float scale, int causal,
                   const KernelCtl& ctl, cudaStream_t st) {
   switch (d) {
-    case 64: return launch_cfg<64, 128, 2>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
+    case 64: return launch_cfg<64, 64, 1>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
     case 128:
       return launch_cfg<128, 128, 2>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
     case 256: return launch_cfg<256, 64, 1>(Q, K, V, O, LSE, BH, hm, tl, n, scale, causal, ctl, st);
