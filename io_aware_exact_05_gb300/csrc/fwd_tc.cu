@@ -69,6 +69,14 @@ struct FwdCfg {
 // Barrier indices inside the barrier block.
 enum : int { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17,
              B_DRAIN = 19, B_QC = 20, B_COUNT = 21 };   // B_QC: Q copied to tensor memory
+// The barrier block holds at most three K and three V ring stages (and 24
+// barriers of 8 bytes below the tensor-memory slot at +192).
+template <class C>
+struct FitsBarrierBlock {
+  static constexpr bool value = C::KSTK <= B_KE - B_KF && C::KSTK <= B_VF - B_KE &&
+                                C::KSTV <= B_VE - B_VF && C::KSTV <= B_SF - B_VE &&
+                                B_COUNT * 8 <= 192;
+};
 
 struct TileInfo {
   int last0, last1;   // last KV tile index each query tile needs (-1: none)
@@ -120,6 +128,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               float* __restrict__ LSE, HeadMap hm, TileLists tl, int n, float scale_log2,
               int causal, KernelCtl ctl) {
   using C = FwdCfg<D, BN, QT>;
+  static_assert(FitsBarrierBlock<C>::value, "ring deeper than its barrier slots");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
