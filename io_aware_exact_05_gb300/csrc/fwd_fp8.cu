@@ -80,6 +80,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                const float* __restrict__ dsk, const float* __restrict__ dsv, int n,
                float scale_log2_base, int causal, KernelCtl ctl) {
   using C = Fp8Cfg;
+  static_assert(C::KST <= F_KE - F_KF && C::KST <= F_VF - F_KE && C::VST <= F_VE - F_VF &&
+                    C::VST <= F_SF - F_VE,
+                "ring deeper than its barrier slots");
   constexpr int D = C::D, BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
