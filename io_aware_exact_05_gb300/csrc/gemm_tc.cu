@@ -25,13 +25,17 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 
-template <int BN>
+template <int BN, int STG = kStages>
 struct GemmLayout {
   static constexpr uint32_t A_BYTES = kBM * kBK * 2;
   static constexpr uint32_t B_BYTES = BN * kBK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
-  static constexpr uint32_t BAR_OFF = kStages * STAGE;
+  static constexpr uint32_t BAR_OFF = STG * STAGE;
   static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;  // barriers + slack for 1 KB alignment
+  // two CTAs per SM when their shared and tensor memory fit (the epilogue of
+  // one then overlaps the loads and MMAs of the other)
+  static constexpr int MINB = (TOTAL <= 232448 / 2 && BN <= 256) ? 2 : 1;
+  static_assert(2 * STG + 2 <= 16, "barriers below the tensor-memory slot");
 };
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -48,11 +52,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int
                 : sdesc_sw128(base + kk * 2048, mn_block_bytes, 1024);
 }
 
-template <int BN, bool A_K, bool B_K, bool C_F32>
-__global__ void __launch_bounds__(128, 1)
+template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages>
+__global__ void __launch_bounds__(128, GemmLayout<BN, STG>::MINB)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                  void* __restrict__ C, int M, int N, int K, float alpha, KernelCtl ctl) {
-  using L = GemmLayout<BN>;
+  using L = GemmLayout<BN, STG>;
+  constexpr int kStages = STG;   // ring depth of this instance
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
   const uint32_t sbase = smem_u32(smem);
@@ -191,11 +196,17 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
   if (warp == 2) tmem_dealloc<BN>(tmem);
 }
 
-template <int BN, bool A_K, bool B_K, bool C_F32>
+template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int batch, int M,
                    int N, int K, float alpha, const KernelCtl& ctl, cudaStream_t st) {
-  auto kern = gemm_bf16_kernel<BN, A_K, B_K, C_F32>;
-  constexpr int smem = GemmLayout<BN>::TOTAL;
+  // short contractions (the n x n score products, K = d <= 256: four K blocks
+  // or fewer) need no deep ring; two stages let two CTAs share an SM so that
+  // one CTA's stores of its fp32 tile overlap the other's MMAs
+  if constexpr (STG == kStages && C_F32 && A_K && B_K) {
+    if (K <= 4 * kBK) return launch_variant<BN, A_K, B_K, C_F32, 2>(ta, tb, C, batch, M, N, K, alpha, ctl, st);
+  }
+  auto kern = gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG>;
+  constexpr int smem = GemmLayout<BN, STG>::TOTAL;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(N, BN), ceil_div(M, kBM), batch);
