@@ -395,7 +395,7 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     mode = {"atomic": attn.ATTN_DQ_ATOMIC, "pass": attn.ATTN_DQ_PASS,
-            "auto": attn.ATTN_DQ_AUTO}[args.mode]
+            "spill": attn.ATTN_DQ_SPILL, "auto": attn.ATTN_DQ_AUTO}[args.mode]
     mode_used = dq_mode_used(args.mode, w.d)
     wr = rank_workload(w, rank)
     x = make_inputs(wr)
@@ -513,7 +513,8 @@ def run_ours(args, w):
     if rank == 0:
         kv_ms = stage_ms[2]
         # the key-tile kernel does all five backward products when it also
-        # forms dQ (atomic mode), four of them (S, dP, dV, dK) in pass mode
+        # forms dQ (atomic mode), four of them (S, dP, dV, dK) in the pass and
+        # spill modes (dQ by the query-tile pass or by a GEMM over dS)
         kv_flops = fl["bwd"] if mode_used == "atomic" else fl["bwd"] * 8 // 10
         achieved = kv_flops / (kv_ms * 1e-3) / 1e12
         peak = float(pk["bf16_tflops"])
@@ -711,8 +712,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", default="auto", choices=["atomic", "pass", "auto"],
-                    help="dQ mode; auto: atomic for d <= 128, the dQ pass above")
+    ap.add_argument("--mode", default="auto", choices=["atomic", "pass", "spill", "auto"],
+                    help="dQ mode; auto: atomic for d <= 128, the dQ pass above; spill: "
+                         "d = 256 non-causal only, dS through the workspace and a GEMM")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0,

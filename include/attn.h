@@ -60,8 +60,16 @@ typedef enum {
   ATTN_DQ_AUTO = 0,   /* the measured default for the shape */
   ATTN_DQ_ATOMIC = 1, /* key-tile kernel adds its dQ share into an fp32
                          workspace accumulator with atomics, then converts */
-  ATTN_DQ_PASS = 2    /* separate query-tile kernel recomputes S, dP, dS and
+  ATTN_DQ_PASS = 2,   /* separate query-tile kernel recomputes S, dP, dS and
                          sums dQ with no atomics */
+  ATTN_DQ_SPILL = 3   /* d = 256, non-causal, dense, one key/value head per
+                         query head: the key-tile kernel also writes dS^T
+                         (bf16, n x n per head) to the workspace and dQ =
+                         scale dS K is one tensor-core GEMM; the workspace
+                         grows by B*H*n*round_up(n, 8)*2 bytes.  Trades the
+                         pass's second recomputation of S and dP for one
+                         n x n write and read through HBM.
+                         ATTN_ERR_UNSUPPORTED for other shapes. */
 } attn_dq_mode;
 
 typedef enum {

@@ -13,7 +13,7 @@ import threading
 import torch
 
 __all__ = [
-    "ATTN_BF16", "ATTN_F32", "ATTN_DQ_AUTO", "ATTN_DQ_ATOMIC", "ATTN_DQ_PASS",
+    "ATTN_BF16", "ATTN_F32", "ATTN_DQ_AUTO", "ATTN_DQ_ATOMIC", "ATTN_DQ_PASS", "ATTN_DQ_SPILL",
     "AttnError", "lib", "lib_path",
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_bwd_dkdv_keys",
@@ -30,7 +30,7 @@ __all__ = [
 ATTN_BF16, ATTN_F32 = 0, 1
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA,
  ATTN_ERR_DEVICE_TIMEOUT) = range(6)
-ATTN_DQ_AUTO, ATTN_DQ_ATOMIC, ATTN_DQ_PASS = 0, 1, 2
+ATTN_DQ_AUTO, ATTN_DQ_ATOMIC, ATTN_DQ_PASS, ATTN_DQ_SPILL = 0, 1, 2, 3
 
 _LIB = None
 _LOCK = threading.Lock()

@@ -58,6 +58,8 @@ struct BwdWorkspace {
   float* lse2;
   float* delta;
   float* dq_acc;
+  void* ds_t;      // bf16 [B*H][n][ld_ds] dS^T (ATTN_DQ_SPILL)
+  int ld_ds;
   float* dk_acc;   // fp32 [B][H_kv][n][d] when gsplit > 1
   float* dv_acc;
   int gsplit;
@@ -82,6 +84,11 @@ BwdWorkspace carve_bwd(void* base, int B, int H, int H_kv, int n, int d, attn_dt
     if (mode == ATTN_DQ_ATOMIC) {
       w.dq_acc = reinterpret_cast<float*>(p + off);
       off += round_up((size_t)BH * n * d * 4, kAlign);
+    }
+    if (mode == ATTN_DQ_SPILL) {
+      w.ld_ds = (int)round_up(n, 8);
+      w.ds_t = p + off;
+      off += round_up((size_t)BH * n * w.ld_ds * 2, kAlign);
     }
     w.gsplit = group_split(B, H, H_kv, n, d, dtype);
     if (w.gsplit > 1) {
@@ -210,18 +217,20 @@ size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int
                                attn_dq_mode mode) {
   if (check_common(B, H, n, d, 1.0f, causal) != ATTN_OK) return 0;
   if (dtype == ATTN_F32) {
-    if (d > 256) return 0;
+    if (d > 256 || mode == ATTN_DQ_SPILL) return 0;
     return carve_bwd(nullptr, B, H, H, n, d, dtype, mode).bytes;
   }
   if (dtype != ATTN_BF16 || !bf16_head_dim(d)) return 0;
   const attn_dq_mode m = resolve_mode(d, mode);
   if (m == ATTN_DQ_ATOMIC && d > 128) return 0;
+  if (m == ATTN_DQ_SPILL && (d != 256 || causal)) return 0;
   return carve_bwd(nullptr, B, H, H, n, d, dtype, m).bytes;
 }
 
 size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int n, int d, attn_dtype dtype,
                                    int causal, attn_dq_mode mode) {
   if (H_kv < 1 || H % H_kv != 0) return 0;
+  if (mode == ATTN_DQ_SPILL && H_kv != H) return 0;
   const size_t mha = attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode);
   if (mha == 0) return 0;
   const attn_dq_mode m = dtype == ATTN_BF16 ? resolve_mode(d, mode) : mode;
@@ -236,15 +245,19 @@ static int bwd_setup(int B, int H, int H_kv, int n, int d, attn_dtype dtype, flo
   int rc = check_common(B, H, n, d, scale, causal);
   if (rc) return rc;
   if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (mode != ATTN_DQ_AUTO && mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_PASS)
+  if (mode != ATTN_DQ_AUTO && mode != ATTN_DQ_ATOMIC && mode != ATTN_DQ_PASS &&
+      mode != ATTN_DQ_SPILL)
     return ATTN_ERR_INVALID_ARG;
   if (dtype == ATTN_F32) {
     if (d > 256) return ATTN_ERR_UNSUPPORTED;
+    if (mode == ATTN_DQ_SPILL) return ATTN_ERR_UNSUPPORTED;
     *resolved = mode;
   } else if (dtype == ATTN_BF16) {
     if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
     *resolved = resolve_mode(d, mode);
     if (*resolved == ATTN_DQ_ATOMIC && d > 128) return ATTN_ERR_UNSUPPORTED;
+    if (*resolved == ATTN_DQ_SPILL && (d != 256 || causal || H_kv != H))
+      return ATTN_ERR_UNSUPPORTED;
   } else {
     return ATTN_ERR_INVALID_ARG;
   }
@@ -334,9 +347,11 @@ static int bwd_dkdv_impl(const void* Q, const void* K, const void* V, const void
         cudaMemsetAsync(w.dv_acc, 0, kv_elems * 4, st) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
+  if (m == ATTN_DQ_SPILL && tl.lists) return ATTN_ERR_UNSUPPORTED;
   rc = launch_bwd_kv_tc(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr, dK,
                         dV, w.dk_acc, w.dv_acc, B * H, HeadMap{H, H / H_kv}, w.gsplit, tl, n,
-                        (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
+                        (int)round_up(n, 128), d, scale, causal, default_ctl(), st,
+                        m == ATTN_DQ_SPILL ? w.ds_t : nullptr, w.ld_ds);
   if (rc || w.gsplit == 1) return rc;
   rc = cuda_rc(launch_dq_convert(w.dk_acc, dK, kv_elems, st));
   if (rc) return rc;
@@ -356,6 +371,12 @@ static int bwd_dq_impl(const void* Q, const void* K, const void* V, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;   // use attn_bwd
   if (m == ATTN_DQ_ATOMIC) return cuda_rc(launch_dq_convert(w.dq_acc, dQ, (size_t)B * H * n * d, st));
+  if (m == ATTN_DQ_SPILL) {   // dQ = scale dS K: A = dS stored as dS^T rows (MN-major), B = K
+    if (tl.lists) return ATTN_ERR_UNSUPPORTED;
+    if (!ptrs_ok({K})) return ATTN_ERR_INVALID_ARG;
+    return launch_gemm_bf16(w.ds_t, K, dQ, B * H, n, d, n, false, false, false, scale,
+                            default_ctl(), st, w.ld_ds);
+  }
   if (!ptrs_ok({Q, K, V, dO})) return ATTN_ERR_INVALID_ARG;
   return launch_bwd_q_tc(Q, K, V, dO, w.lse2, w.delta, dQ, B * H, HeadMap{H, H / H_kv}, tl, n,
                          (int)round_up(n, 128), d, scale, causal, default_ctl(), st);
@@ -380,6 +401,7 @@ int attn_bwd_dkdv_keys(const void* Q, const void* K, const void* V, const void* 
   if (rc) return rc;
   if (dtype == ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (d <= 128 && m != ATTN_DQ_ATOMIC) return ATTN_ERR_UNSUPPORTED;
+  if (m == ATTN_DQ_SPILL) return ATTN_ERR_UNSUPPORTED;   // study instances: dQ by the pass
   return launch_bwd_kv_study(Q, K, V, dO, w.lse2, w.delta, m == ATTN_DQ_ATOMIC ? w.dq_acc : nullptr,
                              dK, dV, B * H, key_rows, n, (int)round_up(n, 128), d, scale, causal,
                              default_ctl(), static_cast<cudaStream_t>(stream));
@@ -410,6 +432,7 @@ static int bwd_impl(const void* Q, const void* K, const void* V, const void* O, 
                     const uint8_t* mask, void* workspace, size_t workspace_bytes, void* stream) {
   if (!ptrs_ok({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID_ARG;
   if (mask && H_kv != H) return ATTN_ERR_UNSUPPORTED;
+  if (mask && mode == ATTN_DQ_SPILL) return ATTN_ERR_UNSUPPORTED;
   attn_dq_mode m;
   BwdWorkspace w;
   int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,

@@ -539,8 +539,10 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int gi = 0, u = 0; go && gi < gper; ++gi) {
       const int bq = qbase + gi;
       for (int ut = 0; ut < cnt; ++ut, ++u) {
-        bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
-        if (!__all_sync(0xffffffffu, ok)) {
+        // both warps of the half take the same branch: they meet at named
+        // barriers below, which have no time limit
+        const bool ok = mbar_wait(bar(B_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
+        if (!named_bar_and(1 + half, 64, ok)) {
           go = false;
           break;
         }

@@ -119,7 +119,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
               __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
               float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n, int n_pad,
-              float scale, float scale_log2, int causal, KernelCtl ctl) {
+              float scale, float scale_log2, int causal, KernelCtl ctl,
+              __nv_bfloat16* __restrict__ dSt, int ld_ds) {
   using C = KvCfg<D, DQ>;
   static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED && !DQ),
                 "owned key rows: a dense, one-head-per-head study instance");
@@ -409,6 +410,20 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = ds[c0 + i];
           tmem_st16(dp_addr + c0, pk);
+        }
+        if (!GROUPED && !SPARSE && dSt != nullptr && key < n && (KR == C::BNK || r < KR)) {
+          // dS^T row of this key, queries [qbase, qbase + NC): dQ = scale dS K
+          // is then one GEMM (the dQ mode "spill"); rows are 16-byte aligned
+          __nv_bfloat16* row = dSt + ((size_t)bh * n + key) * ld_ds + qbase;
+          if (qbase + NC <= n) {
+#pragma unroll
+            for (int c = 0; c < NC / 8; ++c)
+              reinterpret_cast<uint4*>(row)[c] =
+                  make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
+          } else {
+            for (int c = 0; qbase + c < n; ++c)
+              row[c] = __ushort_as_bfloat16((unsigned short)(ds[c >> 1] >> (16 * (c & 1))));
+          }
         }
         tmem_st_wait();
         if (C::WITH_DQ) {
@@ -782,7 +797,8 @@ template <int D, bool DQ, int KR = 128>
 int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
                   const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
                   int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
-                  float scale, int causal, const KernelCtl& ctl, cudaStream_t st) {
+                  float scale, int causal, const KernelCtl& ctl, cudaStream_t st,
+                  void* dSt = nullptr, int ld_ds = 0) {
   using C = KvCfg<D, DQ>;
   const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
@@ -808,7 +824,8 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
                                            gsplit, tl, n, n_pad, scale,
-                                           scale * 1.4426950408889634f, causal, ctl);
+                                           scale * 1.4426950408889634f, causal, ctl,
+                                           static_cast<__nv_bfloat16*>(dSt), ld_ds);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -843,12 +860,15 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
                      const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
                      float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
                      const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
-                     const KernelCtl& ctl, cudaStream_t st) {
+                     const KernelCtl& ctl, cudaStream_t st, void* dSt, int ld_ds) {
   if (gsplit < 1 || hm.group % gsplit != 0 || (gsplit > 1 && (!dKacc || !dVacc)))
     return ATTN_ERR_INVALID_ARG;
+  if (dSt && (d != 256 || hm.group != 1 || tl.lists || causal || ld_ds < n || ld_ds % 8 ||
+              (reinterpret_cast<uintptr_t>(dSt) & 15u)))
+    return ATTN_ERR_UNSUPPORTED;
 #define ATTN_KV(DD, DQQ)                                                                      \
   return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm,    \
-                                gsplit, tl, n, n_pad, scale, causal, ctl, st)
+                                gsplit, tl, n, n_pad, scale, causal, ctl, st, dSt, ld_ds)
   const bool dq = dQacc != nullptr;
   switch (d) {
     case 64:

@@ -6,7 +6,10 @@
 // K blocks of A and B into a 4-stage shared-memory ring with TMA; warp 1
 // (one lane) issues tcgen05.mma (M=128, N=BN, K=16) per K block and releases
 // each stage with tcgen05.commit; then all four warps read the accumulator
-// back with tcgen05.ld (thread t <-> row t) and store C.  A and B may each be
+// back with tcgen05.ld (thread t <-> row t) and store C: through a ring of
+// 128-byte-swizzled 16 KB shared-memory boxes (the drained stage ring) and
+// TMA tile stores when C's rows are 16-byte multiples, else directly from
+// registers.  A and B may each be
 // K-major or MN-major in global memory: the shared-memory descriptors and the
 // transpose bits of the instruction descriptor absorb the difference, so no
 // operand is ever transposed in memory.  This GEMM carries every n x n and
@@ -52,10 +55,11 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int
                 : sdesc_sw128(base + kk * 2048, mn_block_bytes, 1024);
 }
 
-template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages>
+template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages, bool TMA_C = true>
 __global__ void __launch_bounds__(128, GemmLayout<BN, STG>::MINB)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                 void* __restrict__ C, int M, int N, int K, float alpha, KernelCtl ctl) {
+                 const __grid_constant__ CUtensorMap tC, void* __restrict__ C, int M, int N, int K,
+                 float alpha, KernelCtl ctl) {
   using L = GemmLayout<BN, STG>;
   constexpr int kStages = STG;   // ring depth of this instance
   extern __shared__ uint8_t smem_raw[];
@@ -148,9 +152,60 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
   __syncwarp();
 
   // ---------------- epilogue: TMEM -> registers -> global
-  const bool ok = mbar_wait(acc_bar, 0, abort_flag, ctl, SITE_GEMM_ACC);
+  // one verdict for the whole CTA: the TMA epilogue's named barriers need
+  // every thread, so no thread may leave on its own
+  const bool ok = __syncthreads_and(mbar_wait(acc_bar, 0, abort_flag, ctl, SITE_GEMM_ACC)) != 0;
   tc_fence_after();
-  if (ok) {
+  if (TMA_C && ok) {
+    // Every MMA has completed, so the stage ring is free: it holds NBOX boxes
+    // of [128 rows][128 bytes] (32 fp32 or 64 bf16 columns), thread r writing
+    // row r; one thread stores each box with TMA and keeps NBOX - 1 stores
+    // reading shared memory while the next box is written.
+    constexpr uint32_t BOX = kBM * 128;
+    constexpr int COLS = C_F32 ? 32 : 64;
+    constexpr int NBOX = (int)((L::BAR_OFF / BOX) < 4 ? (L::BAR_OFF / BOX) : 4);
+    static_assert(NBOX >= 2, "two staging boxes at least");
+    const int r = warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    int slot = 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN && n0 + c0 < N; c0 += COLS) {
+      uint32_t w[32];
+      if (C_F32) {
+        tmem_ld32(taddr + c0, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(alpha * __uint_as_float(w[i]));
+      } else {
+        uint32_t a[32], bb[32];
+        tmem_ld32(taddr + c0, a);
+        tmem_ld32(taddr + c0 + 32, bb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          w[i] = pack_bf16x2(alpha * __uint_as_float(a[2 * i]), alpha * __uint_as_float(a[2 * i + 1]));
+          w[16 + i] = pack_bf16x2(alpha * __uint_as_float(bb[2 * i]),
+                                  alpha * __uint_as_float(bb[2 * i + 1]));
+        }
+      }
+      uint8_t* box = smem + slot * BOX;
+      if (threadIdx.x == 0) bulk_wait_read<NBOX - 1>();   // this box's last store has read it
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(box + sw128_offset(r, j)) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 0) {
+        tma_store_3d(&tC, smem_u32(box), n0 + c0, m0, b);
+        bulk_commit_group();
+      }
+      slot = (slot + 1 == NBOX) ? 0 : slot + 1;
+    }
+    if (threadIdx.x == 0) bulk_wait_all();   // the stores are complete before the CTA exits
+  }
+  if (!TMA_C && ok) {
     const int row = m0 + warp * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
@@ -205,12 +260,21 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int ba
   if constexpr (STG == kStages && C_F32 && A_K && B_K) {
     if (K <= 4 * kBK) return launch_variant<BN, A_K, B_K, C_F32, 2>(ta, tb, C, batch, M, N, K, alpha, ctl, st);
   }
-  auto kern = gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG>;
+  // C through TMA tile stores when its rows are 16-byte multiples (the
+  // tensor map's stride rule) and its base is 16-byte aligned
+  CUtensorMap tc;
+  const bool tma_c =
+      (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N * (C_F32 ? 4 : 2)) % 16 == 0 &&
+      (C_F32 ? make_tmap_f32(&tc, C, N, M, batch, 32, kBM, true)
+             : make_tmap_bf16(&tc, C, N, M, batch, 64, kBM));
+  if (!tma_c) tc = ta;   // not read
+  auto kern = tma_c ? gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, true>
+                    : gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, false>;
   constexpr int smem = GemmLayout<BN, STG>::TOTAL;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   dim3 grid(ceil_div(N, BN), ceil_div(M, kBM), batch);
-  kern<<<grid, 128, smem, st>>>(ta, tb, C, M, N, K, alpha, ctl);
+  kern<<<grid, 128, smem, st>>>(ta, tb, tc, C, M, N, K, alpha, ctl);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -238,12 +302,12 @@ int dispatch_bn(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int batch
 
 int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, int N, int K,
                      bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
-                     cudaStream_t st) {
+                     cudaStream_t st, int lda) {
   const int BN = N > 128 ? 256 : 128;
   CUtensorMap ta, tb;
   // A: K-major [b][M][K] (x = K) or MN-major [b][K][M] (x = M)
-  bool ok = a_kmajor ? make_tmap_bf16(&ta, A, K, M, batch, 64, kBM)
-                     : make_tmap_bf16(&ta, A, M, K, batch, 64, kBK);
+  bool ok = a_kmajor ? make_tmap_bf16(&ta, A, K, M, batch, 64, kBM, lda)
+                     : make_tmap_bf16(&ta, A, M, K, batch, 64, kBK, lda);
   // B: K-major [b][N][K] (x = K) or MN-major [b][K][N] (x = N)
   ok = ok && (b_kmajor ? make_tmap_bf16(&tb, B, K, N, batch, 64, BN)
                        : make_tmap_bf16(&tb, B, N, K, batch, 64, kBK));

@@ -67,11 +67,12 @@ unsigned long long current_context_id() {
 }
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
-                    uint32_t box_x, uint32_t box_y) {
+                    uint32_t box_x, uint32_t box_y, uint64_t ld) {
   auto fn = encode_fn();
   if (!fn) return false;
+  if (ld == 0) ld = x;
   const cuuint64_t dims[3] = {x, y, z};
-  const cuuint64_t strides[2] = {x * 2, x * y * 2};   // bytes, dims 1..2
+  const cuuint64_t strides[2] = {ld * 2, ld * y * 2};   // bytes, dims 1..2
   const cuuint32_t box[3] = {box_x, box_y, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,

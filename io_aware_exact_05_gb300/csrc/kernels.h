@@ -13,8 +13,9 @@ namespace attn {
 // ---- tensor maps (host) ---------------------------------------------------
 // A 3-D bf16 tensor map over [z][y][x] (x innermost, contiguous), with the
 // 128-byte swizzle and zero fill outside the tensor.  box_x * 2 must be 128.
+// Rows are ld elements apart (ld = 0: packed, ld = x; ld * 2 a multiple of 16).
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
-                    uint32_t box_x, uint32_t box_y);
+                    uint32_t box_x, uint32_t box_y, uint64_t ld = 0);
 // A 3-D 8-bit tensor map over [z][y][x], 128-byte swizzle, zero fill outside
 // the tensor (box_x must be 128; x a multiple of 16).
 bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t x, uint64_t y, uint64_t z,
@@ -74,9 +75,10 @@ cudaError_t launch_delta_bf16(const void* O, const void* dO, const float* LSE, f
 cudaError_t launch_dq_convert(const float* acc, void* dQ, size_t elems, cudaStream_t st);
 
 // ---- tensor-core kernels -------------------------------------------------------
+// lda: row length of A in elements (0: packed); batches of A lda * rows apart.
 int launch_gemm_bf16(const void* A, const void* B, void* C, int batch, int M, int N, int K,
                      bool a_kmajor, bool b_kmajor, bool c_f32, float alpha, const KernelCtl& ctl,
-                     cudaStream_t st);
+                     cudaStream_t st, int lda = 0);
 
 // tl.lists != null: block-sparse (one key/value head per query head only).
 int launch_fwd_tc(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH,
@@ -94,11 +96,14 @@ void fwd_tiling(int d, int* query_rows, int* query_tiles, int* kv_rows);
 // caller; dK already scaled), which the caller converts.
 // tl.lists != null: block-sparse, each key tile walking its listed query
 // tiles (one key/value head per query head only).
+// dSt (d = 256, dense, one key/value head per query head, non-causal only):
+// the dK CTAs also store dS^T in bf16, [BH][n keys][ld_ds queries], for dQ by
+// a GEMM afterwards.
 int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO,
                      const float* LSE2, const float* Dv, float* dQacc, void* dK, void* dV,
                      float* dKacc, float* dVacc, int BH, const HeadMap& hm, int gsplit,
                      const TileLists& tl, int n, int n_pad, int d, float scale, int causal,
-                     const KernelCtl& ctl, cudaStream_t st);
+                     const KernelCtl& ctl, cudaStream_t st, void* dSt = nullptr, int ld_ds = 0);
 // Tiling of the key-tile kernel for head dim d (key tiles of kv_rows keys,
 // query tiles of query_rows).
 void bwd_kv_tiling(int d, int* kv_rows, int* query_rows);

@@ -52,6 +52,9 @@ block-sparse forward and backward over make_block_mask(n, W, G, R) (seed
 recomputes Z_QK from the same pattern and takes Z_in = n d (the inputs are
 dense; with Z_QK = n^2 both terms become Theorem 1.1's).
 
+`time --path fused|mat` times warm forward and backward calls of one path
+with CUDA events (no profiler), for the fused vs materialise-P comparison.
+
 `kernels` reads a launch list taken with
 `ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum`
 and prints, per launch, its time, DRAM bytes and DRAM GB/s against the
@@ -116,6 +119,54 @@ def _run(path, n, d, b=B, h=H, causal=False, dtype="bf16", key_rows=0, pattern=N
     rc = attn.attn_status()
     if rc:
         raise SystemExit("device status %d" % rc)
+
+
+def _time(path, n, d, b, h, causal, reps=10):
+    """Mean ms of the forward and of the backward of one path, warm, CUDA events."""
+    import torch
+
+    from . import attn
+    from .inputs import Workload, make_inputs
+
+    w = Workload("io", b, h, n, d, "bf16", causal, 1.0, 2000 + n + d)
+    x = make_inputs(w)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (x[t].to(dev) for t in ("q", "k", "v", "do"))
+    o, lse = torch.empty_like(q), torch.empty(b, h, n, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if path == "mat":
+        ws = torch.empty(attn.attn_mat_workspace_size(b, h, n, d), dtype=torch.uint8, device=dev)
+        fwd = lambda: attn.attn_mat_fwd(q, k, v, o, lse, w.scale, causal, ws)   # noqa: E731
+        bwd = lambda: attn.attn_mat_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, causal, ws)  # noqa: E731
+    else:
+        mode = attn.ATTN_DQ_AUTO
+        ws = torch.empty(attn.attn_bwd_workspace_size(b, h, n, d, attn.ATTN_BF16, causal, mode),
+                         dtype=torch.uint8, device=dev)
+        fwd = lambda: attn.attn_fwd(q, k, v, o, lse, w.scale, causal)   # noqa: E731
+        bwd = lambda: attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.scale, causal, mode, ws)  # noqa: E731
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    tf = tb = 0.0
+    for _ in range(reps):
+        ev[0].record()
+        fwd()
+        ev[1].record()
+        bwd()
+        ev[2].record()
+        torch.cuda.synchronize()
+        tf += ev[0].elapsed_time(ev[1])
+        tb += ev[1].elapsed_time(ev[2])
+    if attn.attn_status():
+        raise SystemExit("device status error")
+    fl = 4 * b * h * n * n * d // (2 if causal else 1)
+    out = {"path": path, "B": b, "H": h, "n": n, "d": d, "causal": causal,
+           "fwd_ms": tf / reps, "bwd_ms": tb / reps,
+           "fwd_tflops": fl / (tf / reps * 1e-3) / 1e12,
+           "bwd_tflops": 2.5 * fl / (tb / reps * 1e-3) / 1e12}
+    print(json.dumps(out))
 
 
 def _rows(path):
@@ -279,6 +330,13 @@ def main(argv=None):
     r.add_argument("--key-rows", type=int, default=0, choices=[0, 32, 64, 128],
                    help="fused bf16 backward with key tiles of this many keys (0: the product "
                         "kernels through attn_bwd)")
+    tm = sub.add_parser("time")
+    tm.add_argument("--path", choices=["fused", "mat"], required=True)
+    tm.add_argument("--n", type=int, required=True)
+    tm.add_argument("--d", type=int, required=True)
+    tm.add_argument("--B", type=int, default=B)
+    tm.add_argument("--H", type=int, default=H)
+    tm.add_argument("--causal", action="store_true")
     kr = sub.add_parser("keyrows")
     kr.add_argument("csv", nargs="+")
     sp = sub.add_parser("sparse")
@@ -291,6 +349,8 @@ def main(argv=None):
     if a.cmd == "run":
         _run(a.path, a.n, a.d, a.B, a.H, a.causal, a.dtype, a.key_rows,
              tuple(int(x) for x in a.pattern.split(",")))
+    elif a.cmd == "time":
+        _time(a.path, a.n, a.d, a.B, a.H, a.causal)
     elif a.cmd == "keyrows":
         _keyrows(a.csv)
     elif a.cmd == "sparse":

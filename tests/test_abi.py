@@ -177,6 +177,34 @@ def test_key_rows_study_argument_checks(L):
     assert L.attn_launch_count() == before
 
 
+def test_dq_spill_mode_checks(L):
+    """ATTN_DQ_SPILL (3): d = 256, non-causal, dense, one key/value head per
+    query head; its workspace adds a bf16 n x round_up(n, 8) dS^T per head."""
+    ws = ctypes.c_void_p(1 << 24)
+    B, H, n = 1, 2, 300
+    pas = L.attn_bwd_workspace_size(B, H, n, 256, 0, 0, 2)
+    spill = L.attn_bwd_workspace_size(B, H, n, 256, 0, 0, 3)
+    ld = (n + 7) // 8 * 8
+    assert spill >= pas + B * H * n * ld * 2 and spill - pas < B * H * n * ld * 2 + 512
+    assert L.attn_bwd_workspace_size(B, H, n, 256, 0, 1, 3) == 0      # causal
+    assert L.attn_bwd_workspace_size(B, H, n, 128, 0, 0, 3) == 0      # d <= 128
+    assert L.attn_bwd_workspace_size(B, H, n, 256, 1, 0, 3) == 0      # fp32
+    assert L.attn_bwd_gqa_workspace_size(B, 4, 2, n, 256, 0, 0, 3) == 0
+    before = L.attn_launch_count()
+
+    def bwd(*, d=256, causal=0, mode=3, dt=0):
+        return L.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, n, d, dt,
+                          0.1, causal, mode, ws, 1 << 30, None)
+
+    assert bwd(causal=1) == 2 and bwd(d=128) == 2 and bwd(dt=1) == 2
+    assert bwd(mode=4) == 1
+    assert L.attn_bwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, 4, 2, n, 256, 0,
+                          0.1, 0, 3, ws, 1 << 30, None) == 2
+    assert L.attn_bwd_sparse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, n, 256, 0,
+                             0.1, 0, 3, FAKE, ws, 1 << 30, None) == 2
+    assert L.attn_launch_count() == before
+
+
 def test_gqa_argument_checks(L):
     def fwd(H=4, Hkv=2, d=64):
         return L.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, H, Hkv, 128, d, 0, 0.125, 0, None)

@@ -45,3 +45,20 @@ def test_gemm_ragged_kmajor(cuda_dev):
     attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, 1, 1)
     assert attn.attn_status() == 0
     assert relerr(c, ref) <= 1e-5
+
+
+@pytest.mark.parametrize("M,N,c_f32", [(130, 72, True), (130, 70, True), (200, 72, False),
+                                       (200, 68, False), (257, 40, True)])
+def test_gemm_ragged_epilogues(cuda_dev, M, N, c_f32):
+    # C rows that are 16-byte multiples go out through TMA tile stores (rows
+    # and columns past C's edge clipped by the tensor map), others through
+    # direct stores: both, with ragged M and N
+    from io_aware_exact_05_gb300 import attn
+
+    batch, K = 2, 48
+    a, b, ref = _operands(batch, M, N, K, 1, 1, seed=M + N)
+    c = torch.full((batch, M, N), float("nan"), device=cuda_dev,
+                   dtype=torch.float32 if c_f32 else torch.bfloat16)
+    attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, 1, 1)
+    assert attn.attn_status() == 0
+    assert relerr(c, ref) <= (1e-5 if c_f32 else 1e-2)
