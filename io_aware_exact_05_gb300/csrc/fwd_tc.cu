@@ -12,7 +12,9 @@
 //                      into separate shared-memory rings.
 //   warp 1 (one lane)  MMA issuer: S = Q K_j^T (SS-MMA into a TMEM slot),
 //                      O_t += P V_j (TS-MMA: P read from TMEM).
-//   warp 2             allocates / frees tensor memory.
+//   warp 2             allocates / frees tensor memory; in block-sparse
+//                      launches with two query tiles, warps 1 and 2 each
+//                      issue the MMAs of one tile.
 //   warpgroup 1 + t    softmax of query tile t: thread r owns row r (TMEM
 //                      lane r).  Loads its S row, applies the causal/ragged
 //                      mask, updates the running max m and sum l (log2
@@ -68,7 +70,8 @@ struct FwdCfg {
 
 // Barrier indices inside the barrier block.
 enum : int { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17,
-             B_DRAIN = 19, B_QC = 20, B_COUNT = 21 };   // B_QC: Q copied to tensor memory
+             B_DRAIN = 19, B_QC = 20, B_DRAIN1 = 21, B_COUNT = 22 };
+// B_QC: Q copied to tensor memory; B_DRAIN1: the second issuer's drain
 // The barrier block holds at most three K and three V ring stages (and 24
 // barriers of 8 bytes below the tensor-memory slot at +192).
 template <class C>
@@ -129,6 +132,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               int causal, KernelCtl ctl) {
   using C = FwdCfg<D, BN, QT>;
   static_assert(FitsBarrierBlock<C>::value, "ring deeper than its barrier slots");
+  // Block-sparse, two query tiles: one MMA-issuing warp per tile (warps 1
+  // and 2), each tile with its own S slot, so a tile whose list entry is not
+  // kept never waits behind the other tile's units (A/B on
+  // b2h16_n16k_d128_sparse: 0.394 -> 0.346 ms).  Dense launches keep one
+  // issuer with S ping-ponging between the tiles in a fixed unit order (one
+  // issuer per tile was 10 % slower there: each tile's S then completes
+  // later behind the other tile's interleaved MMAs).
+  constexpr bool DUAL = (QT == 2) && SPARSE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -175,11 +186,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(B_Q), 1);
     for (int s = 0; s < C::KSTK; ++s) {
       mbar_init(bar(B_KF + s), 1);
-      mbar_init(bar(B_KE + s), 1);
+      mbar_init(bar(B_KE + s), DUAL ? 2 : 1);   // DUAL: released by both issuers
     }
     for (int s = 0; s < C::KSTV; ++s) {
       mbar_init(bar(B_VF + s), 1);
-      mbar_init(bar(B_VE + s), 1);
+      mbar_init(bar(B_VE + s), DUAL ? 2 : 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SF + s), 1);
@@ -187,6 +198,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar(B_OD + s), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN1), 1);
     mbar_init(bar(B_QC), 128);
     *abort_flag = 0;
     fence_mbar_init();
@@ -256,7 +268,81 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (last_v[s] >= 0)
             mbar_wait(bar(B_VF + s), (last_v[s] / C::KSTV) & 1, &no_abort, ctl, SITE_FWD_V_FULL);
       }
-    } else if (warp == 1) {
+    } else if (DUAL && (warp == 1 || warp == 2)) {
+      // ------------------------------------------- MMA issuer of query tile t
+      // Tile t's S lives in slot t.  Per KV step j: S(t, j) (after K_j
+      // landed), then, once the softmax published P(t, j), PV(t, j) and S(t,
+      // j + 1).  The commit after S(t, j + 1) also covers PV(t, j) (a commit
+      // tracks every earlier MMA of its thread), so only the tile's last PV
+      // is committed on its own.  Each issuer releases a K or V stage once
+      // it has read it, twice when the other tile does not use that stage.
+      const int t = warp - 1;
+      constexpr uint32_t idesc_s = idesc_bf16(C::BM, BN, false, false);   // Q, K both K-major
+      constexpr uint32_t idesc_o = idesc_bf16(C::BM, D, false, true);     // P (TMEM), V MN-major
+      constexpr uint32_t HI = sdesc_hi(1024);
+      const int last = t == 0 ? ti.last0 : ti.last1;
+      const int last_other = t == 0 ? ti.last1 : ti.last0;
+      const uint32_t qb = sdesc_lo(sb + C::Q_OFF, 16) + t * (C::Q_BYTES >> 4);
+      const uint32_t k_lo = sdesc_lo(sb + C::K_OFF, 16);
+      const uint32_t v_lo = sdesc_lo(sb + C::V_OFF, BN * 128);
+      const uint32_t s_col = tmem + C::S_COL + t * BN;
+      bool ok = mbar_wait_warp(bar(B_Q), 0, abort_flag, ctl, SITE_FWD_LOAD_Q);
+      bool drop_s = false, o_init = false;
+      auto issue_s = [&](int j, int ent) -> bool {   // S(t, j) = Q_t K_j^T into slot t
+        const int st = j % C::KSTK;
+        if (!mbar_wait_warp(bar(B_KF + st), (j / C::KSTK) & 1, abort_flag, ctl, SITE_FWD_K_FULL))
+          return false;
+        drop_s = SPARSE && !((ent >> (16 + t)) & 1);
+        tc_fence_after();
+        const uint32_t kb = k_lo + st * (C::KV_BYTES >> 4);
+#pragma unroll
+        for (int b = 0; b < C::NKB; ++b) {
+          if (drop_s) break;
+          uint32_t alo[4], blo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            alo[i] = qb + b * (C::BM * 128 / 16) + 2 * i;
+            blo[i] = kb + b * (BN * 128 / 16) + 2 * i;
+          }
+          mma_ss_x4(s_col, alo, HI, blo, HI, idesc_s, b > 0);
+        }
+        tc_commit(bar(B_SF + t));
+        tc_commit(bar(B_KE + st));
+        if (j > last_other) tc_commit(bar(B_KE + st));
+        return true;
+      };
+      auto entry_of = [&](int j) { return SPARSE ? slist[j] : 0; };
+      if (ok && last >= 0) ok = issue_s(0, entry_of(0));
+      for (int j = 0; ok && j <= last; ++j) {
+        const int sv = j % C::KSTV;
+        const uint32_t vb = v_lo + sv * (C::KV_BYTES >> 4);
+        const int ent1 = (SPARSE && j + 1 <= last) ? entry_of(j + 1) : 0;   // load before the wait
+        if (!mbar_wait_warp(bar(B_PF + t), j & 1, abort_flag, ctl, SITE_FWD_P_FULL)) break;
+        if (!mbar_wait_warp(bar(B_VF + sv), (j / C::KSTV) & 1, abort_flag, ctl, SITE_FWD_V_FULL))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int b = 0; b < BN / 64; ++b) {   // 64 keys (4 MMAs of K = 16) per group
+          if (drop_s) break;
+          uint32_t blo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) blo[i] = vb + (4 * b + i) * (2048 / 16);
+          const bool acc = SPARSE ? (o_init || b > 0) : (j > 0 || b > 0);
+          mma_ts_x4(tmem + C::O_COL + t * D, s_col + 32 * b, blo, HI, idesc_o, acc);
+        }
+        if (SPARSE && !drop_s) o_init = true;
+        if (j == last) tc_commit(bar(B_OD + t));
+        tc_commit(bar(B_VE + sv));
+        if (j > last_other) tc_commit(bar(B_VE + sv));
+        if (j + 1 <= last) ok = issue_s(j + 1, ent1);
+      }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        const int drain = t == 0 ? B_DRAIN : B_DRAIN1;
+        tc_commit(bar(drain));
+        volatile int no_abort = 0;
+        mbar_wait_warp(bar(drain), 0, &no_abort, ctl, SITE_FWD_O_DONE);
+      }
+    } else if (!DUAL && warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs this loop (one elected lane issues each MMA and
       // commit), so every descriptor stays warp-uniform.  Per-unit
@@ -370,8 +456,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
     }
     for (int j = 0; ok && j <= last; ++j) {
-      const int k = unit_pos(t, j, ti);
-      const int slot = k & 1;
+      const int k = DUAL ? 2 * j : unit_pos(t, j, ti);   // DUAL: slot t, phase j
+      const int slot = DUAL ? t : (k & 1);
       const int ent = SPARSE ? slist[j] : j;   // read before the wait hides its latency
       ok = mbar_wait(bar(B_SF + slot), (k >> 1) & 1, abort_flag, ctl, SITE_FWD_S_FULL);
       ok = __all_sync(0xffffffffu, ok);
@@ -437,7 +523,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // completion was implied by the S wait above; otherwise wait for its
       // own commit (every committed phase is waited for, so a parity wait
       // is never more than one phase behind).
-      if (j > 0 && !pv_implied(t, j - 1, ti)) {
+      if (j > 0 && !DUAL && !pv_implied(t, j - 1, ti)) {
         ok = mbar_wait(bar(B_OD + t), odc & 1, abort_flag, ctl, SITE_FWD_O_DONE);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
