@@ -272,13 +272,21 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def dq_mode_used(mode, d):
-    """The dQ mode a bf16 backward runs: "auto" is the reduce-add from the
-    key-tile kernel for d <= 128 and the separate dQ pass above (the library's
-    own rule)."""
+def dq_mode_used(mode, w):
+    """The dQ mode a bf16 backward of workload w runs (the library's own rule
+    for "auto"): the reduce-adds from the key-tile kernel for d <= 128; for
+    d = 256 the spill mode (dS^T through the workspace, one GEMM) when the
+    call is non-causal, dense and one key/value head per query head and the
+    n x n buffer is at most 4 GiB, else the separate dQ pass."""
     if mode != "auto":
         return mode
-    return "atomic" if d <= 128 else "pass"
+    if w.d <= 128:
+        return "atomic"
+    ld = (w.n + 7) // 8 * 8
+    if (not w.causal and not w.sparse and w.kv_heads == w.H
+            and w.B * w.H * w.n * ld * 2 <= 4 << 30):
+        return "spill"
+    return "pass"
 
 
 def traffic_per_launch(w):
@@ -396,7 +404,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     mode = {"atomic": attn.ATTN_DQ_ATOMIC, "pass": attn.ATTN_DQ_PASS,
             "spill": attn.ATTN_DQ_SPILL, "auto": attn.ATTN_DQ_AUTO}[args.mode]
-    mode_used = dq_mode_used(args.mode, w.d)
+    mode_used = dq_mode_used(args.mode, w)
     wr = rank_workload(w, rank)
     x = make_inputs(wr)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))

@@ -57,7 +57,11 @@ typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
 
 /* How attn_bwd combines dQ = scale * sum_j dS_ij k_j across key tiles. */
 typedef enum {
-  ATTN_DQ_AUTO = 0,   /* the measured default for the shape */
+  ATTN_DQ_AUTO = 0,   /* the measured default for the shape: ATTN_DQ_ATOMIC
+                         for d <= 128; for d = 256 ATTN_DQ_SPILL when that
+                         mode applies and its dS^T buffer is at most 4 GiB,
+                         else ATTN_DQ_PASS (the workspace-size functions
+                         make the same choice) */
   ATTN_DQ_ATOMIC = 1, /* key-tile kernel adds its dQ share into an fp32
                          workspace accumulator with atomics, then converts */
   ATTN_DQ_PASS = 2,   /* separate query-tile kernel recomputes S, dP, dS and

@@ -31,12 +31,23 @@ int check_common(int B, int H, int n, int d, float scale, int causal) {
 
 bool bf16_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
-// dQ mode actually used for a bf16 shape.  The key-tile kernel can carry the
-// dQ accumulator in tensor memory only for d <= 128; d = 256 always uses the
-// separate query-tile pass.
-attn_dq_mode resolve_mode(int d, attn_dq_mode mode) {
-  if (mode == ATTN_DQ_AUTO) return d <= 128 ? ATTN_DQ_ATOMIC : ATTN_DQ_PASS;
-  return mode;
+// The automatic dQ mode spills dS^T only while that buffer stays below this.
+constexpr size_t kSpillAutoMaxBytes = size_t(4) << 30;
+
+// dQ mode actually used for a bf16 shape (measured choices).  d <= 128: the
+// key-tile kernel's reduce-adds (1.25-1.48 x faster than the pass).  d = 256:
+// the key-tile kernel has no tensor-memory columns for a dQ tile; the spill
+// mode (dS^T through the workspace, one GEMM) is 17 % faster than the pass
+// where it applies (non-causal, dense, one key/value head per query head)
+// and while its n x n buffer stays under kSpillAutoMaxBytes; else the pass.
+attn_dq_mode resolve_mode(int B, int H, int H_kv, int n, int d, int causal, bool masked,
+                          attn_dq_mode mode) {
+  if (mode != ATTN_DQ_AUTO) return mode;
+  if (d <= 128) return ATTN_DQ_ATOMIC;
+  const size_t spill = (size_t)B * H * n * round_up(n, 8) * 2;
+  if (d == 256 && !causal && !masked && H_kv == H && spill <= kSpillAutoMaxBytes)
+    return ATTN_DQ_SPILL;
+  return ATTN_DQ_PASS;
 }
 
 // CTAs per key/value head for the bf16 key-tile kernel.  A group of query
@@ -221,7 +232,7 @@ size_t attn_bwd_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int
     return carve_bwd(nullptr, B, H, H, n, d, dtype, mode).bytes;
   }
   if (dtype != ATTN_BF16 || !bf16_head_dim(d)) return 0;
-  const attn_dq_mode m = resolve_mode(d, mode);
+  const attn_dq_mode m = resolve_mode(B, H, H, n, d, causal, false, mode);
   if (m == ATTN_DQ_ATOMIC && d > 128) return 0;
   if (m == ATTN_DQ_SPILL && (d != 256 || causal)) return 0;
   return carve_bwd(nullptr, B, H, H, n, d, dtype, m).bytes;
@@ -231,9 +242,11 @@ size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int n, int d, attn_dt
                                    int causal, attn_dq_mode mode) {
   if (H_kv < 1 || H % H_kv != 0) return 0;
   if (mode == ATTN_DQ_SPILL && H_kv != H) return 0;
-  const size_t mha = attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode);
+  // the sizes of the grouped call's own mode (the automatic choice depends on H_kv)
+  const attn_dq_mode m =
+      dtype == ATTN_BF16 ? resolve_mode(B, H, H_kv, n, d, causal, false, mode) : mode;
+  const size_t mha = attn_bwd_workspace_size(B, H, n, d, dtype, causal, m);
   if (mha == 0) return 0;
-  const attn_dq_mode m = dtype == ATTN_BF16 ? resolve_mode(d, mode) : mode;
   return carve_bwd(nullptr, B, H, H_kv, n, d, dtype, m).bytes;
 }
 
@@ -254,7 +267,7 @@ static int bwd_setup(int B, int H, int H_kv, int n, int d, attn_dtype dtype, flo
     *resolved = mode;
   } else if (dtype == ATTN_BF16) {
     if (!bf16_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
-    *resolved = resolve_mode(d, mode);
+    *resolved = resolve_mode(B, H, H_kv, n, d, causal, false, mode);
     if (*resolved == ATTN_DQ_ATOMIC && d > 128) return ATTN_ERR_UNSUPPORTED;
     if (*resolved == ATTN_DQ_SPILL && (d != 256 || causal || H_kv != H))
       return ATTN_ERR_UNSUPPORTED;
@@ -433,6 +446,10 @@ static int bwd_impl(const void* Q, const void* K, const void* V, const void* O, 
   if (!ptrs_ok({Q, K, V, O, dO, LSE, dQ, dK, dV})) return ATTN_ERR_INVALID_ARG;
   if (mask && H_kv != H) return ATTN_ERR_UNSUPPORTED;
   if (mask && mode == ATTN_DQ_SPILL) return ATTN_ERR_UNSUPPORTED;
+  // one resolution for every stage below (the stage entry points resolve for
+  // a dense, one-head-per-head call, which is not this call's shape)
+  if (dtype == ATTN_BF16 && H_kv >= 1 && H % H_kv == 0)
+    mode = resolve_mode(B, H, H_kv, n, d, causal, mask != nullptr, mode);
   attn_dq_mode m;
   BwdWorkspace w;
   int rc = bwd_setup(B, H, H_kv, n, d, dtype, scale, causal, mode, workspace, workspace_bytes, &m,
@@ -487,6 +504,8 @@ int attn_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, con
 
 size_t attn_bwd_sparse_workspace_size(int B, int H, int n, int d, attn_dtype dtype, int causal,
                                       attn_dq_mode mode) {
+  if (mode == ATTN_DQ_SPILL) return 0;
+  if (dtype == ATTN_BF16) mode = resolve_mode(B, H, H, n, d, causal, true, mode);
   const size_t dense = attn_bwd_workspace_size(B, H, n, d, dtype, causal, mode);
   if (dense == 0) return 0;
   return dense + (dtype == ATTN_BF16 ? bwd_lists_bytes(n, d) : 0);

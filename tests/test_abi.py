@@ -89,7 +89,9 @@ def test_workspace_sizes(L):
     assert _ws(L, B, H, n, d, 0, 1, 1) == stats + _rup(BH * n * d * 4)   # atomic
     assert _ws(L, B, H, n, d, 0, 1, 2) == stats                          # pass
     assert _ws(L, B, H, n, d, 0, 1, 0) == _ws(L, B, H, n, d, 0, 1, 1)    # auto = atomic
-    assert _ws(L, B, H, n, 256, 0, 0, 0) == stats                        # d=256: pass
+    assert _ws(L, B, H, n, 256, 0, 1, 0) == stats                        # d=256 causal: pass
+    assert _ws(L, B, H, n, 256, 0, 0, 2) == stats
+    assert _ws(L, B, H, n, 256, 0, 0, 0) == stats + _rup(BH * n * 1000 * 2)   # spill: dS^T
     assert _ws(L, B, H, n, 256, 0, 0, 1) == 0                            # not supported
     assert _ws(L, B, H, n, 100, 1, 0, 0) == _rup(BH * n * 4)             # fp32: D only
     assert _ws(L, B, H, n, 96, 0, 0, 0) == 0
@@ -187,6 +189,15 @@ def test_dq_spill_mode_checks(L):
     ld = (n + 7) // 8 * 8
     assert spill >= pas + B * H * n * ld * 2 and spill - pas < B * H * n * ld * 2 + 512
     assert L.attn_bwd_workspace_size(B, H, n, 256, 0, 1, 3) == 0      # causal
+    # the automatic mode: spill where it applies and its buffer is <= 4 GiB
+    assert L.attn_bwd_workspace_size(B, H, n, 256, 0, 0, 0) == spill
+    assert L.attn_bwd_workspace_size(B, H, n, 256, 0, 1, 0) == L.attn_bwd_workspace_size(B, H, n, 256, 0, 1, 2)
+    assert L.attn_bwd_workspace_size(16, 8, 32768, 256, 0, 0, 0) == \
+        L.attn_bwd_workspace_size(16, 8, 32768, 256, 0, 0, 2)             # 274 GB: the pass
+    assert L.attn_bwd_gqa_workspace_size(B, 4, 2, n, 256, 0, 0, 0) == \
+        L.attn_bwd_gqa_workspace_size(B, 4, 2, n, 256, 0, 0, 2)
+    lists = L.attn_bwd_sparse_workspace_size(B, H, n, 256, 0, 0, 2) - pas
+    assert L.attn_bwd_sparse_workspace_size(B, H, n, 256, 0, 0, 0) == pas + lists
     assert L.attn_bwd_workspace_size(B, H, n, 128, 0, 0, 3) == 0      # d <= 128
     assert L.attn_bwd_workspace_size(B, H, n, 256, 1, 0, 3) == 0      # fp32
     assert L.attn_bwd_gqa_workspace_size(B, 4, 2, n, 256, 0, 0, 3) == 0

@@ -78,9 +78,16 @@ def test_whole_job_rate_and_single_rank_identity():
 
 def test_dq_mode_default_follows_the_library_rule():
     b = _bench()
-    assert b.dq_mode_used("auto", 64) == b.dq_mode_used("auto", 128) == "atomic"
-    assert b.dq_mode_used("auto", 256) == "pass"
-    assert b.dq_mode_used("pass", 128) == "pass" and b.dq_mode_used("atomic", 64) == "atomic"
+    from io_aware_exact_05_gb300.inputs import workload
+
+    w = workload("b2h8_n4k_d256")
+    assert b.dq_mode_used("auto", w.with_shape(d=64)) == b.dq_mode_used("auto", w.with_shape(d=128)) == "atomic"
+    assert b.dq_mode_used("auto", w) == "spill"                          # non-causal, dense, 537 MB
+    assert b.dq_mode_used("auto", w.with_shape(causal=True)) == "pass"
+    assert b.dq_mode_used("auto", w.with_shape(H_kv=4)) == "pass"
+    assert b.dq_mode_used("auto", w.with_shape(sparse=(1, 1, 1))) == "pass"
+    assert b.dq_mode_used("auto", w.with_shape(B=16, n=32768)) == "pass"   # over 4 GiB
+    assert b.dq_mode_used("pass", w) == "pass" and b.dq_mode_used("atomic", w) == "atomic"
 
 
 def test_reference_arm_under_torchrun_prints_once():

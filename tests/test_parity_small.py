@@ -59,7 +59,7 @@ def test_bf16_fused(cuda_dev, d, causal, n):
     _check(w, x, outs, TOL["bf16"])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [129, 520])
 def test_bf16_dq_pass_mode(cuda_dev, d, causal, n):

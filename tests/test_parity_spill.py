@@ -1,8 +1,8 @@
 """The dQ mode "spill" (d = 256): the key-tile kernel also writes dS^T to the
 workspace and dQ = scale dS K is one tensor-core GEMM.  Every element of dQ,
 dK and dV against the float64 oracle on ragged shapes and scales, through
-attn_bwd and through the three stages, and every head of the full d = 256
-workload."""
+attn_bwd and through the three stages; and, since the automatic mode now
+spills on the full d = 256 workload, the query-tile pass on every head of it."""
 
 import pytest
 import torch
@@ -69,13 +69,15 @@ def test_spill_stages_and_scale(cuda_dev, scale):
     _check(w, x, (dq, dk, dv), scale)
 
 
-def test_spill_full_workload_every_head(cuda_dev):
+def test_pass_full_workload_every_head(cuda_dev):
+    # the automatic mode spills on this workload (test_parity_configs checks
+    # it on every head); the query-tile pass, every head, at full size
     from io_aware_exact_05_gb300 import attn
 
     w = workload("b2h8_n4k_d256")
     x = make_inputs(w)
     q, k, v, do = (x[t].to(cuda_dev) for t in ("q", "k", "v", "do"))
     o, lse = attn.forward(q, k, v)
-    outs = attn.backward(q, k, v, o, do, lse, mode=attn.ATTN_DQ_SPILL)
+    outs = attn.backward(q, k, v, o, do, lse, mode=attn.ATTN_DQ_PASS)
     assert attn.attn_status() == 0
     _check(w, x, outs, w.scale, heads=range(w.B * w.H))
