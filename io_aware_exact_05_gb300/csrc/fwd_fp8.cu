@@ -94,15 +94,32 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  // Causal or block-sparse (tiles of unequal length): heads vary fastest in
-  // the grid and tiles slowest, longest first, so the long tiles of every
-  // head start early instead of the last heads' long tiles trailing the rest
-  // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
-  // head's K and V shared in L2 by CTAs that run together.
+  // Causal (tiles of unequal length): heads vary fastest in the grid, in
+  // groups of 8 (the last group may be smaller), and tiles slowest, longest
+  // first, so the long tiles of every head of a group start early while only
+  // that group's K and V are in flight (kept in L2).  Otherwise tiles vary
+  // fastest, which keeps a head's K and V shared in L2 by CTAs that run
+  // together.
   const bool heads_fast = causal;
-  const int bh = heads_fast ? blockIdx.x : blockIdx.y;
+  int head_ix = heads_fast ? blockIdx.x : blockIdx.y;
+  int tile_pos = heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  if (causal) {
+    constexpr int kHeadGroup = 8;
+    const int nh = (int)gridDim.x, nt = (int)gridDim.y;
+    const int L = (int)(blockIdx.x + gridDim.x * blockIdx.y);
+    const int full = nh / kHeadGroup, per = kHeadGroup * nt;
+    if (L < full * per) {
+      tile_pos = (L % per) / kHeadGroup;
+      head_ix = (L / per) * kHeadGroup + (L % per) % kHeadGroup;
+    } else {
+      const int rest = nh - full * kHeadGroup, Lr = L - full * per;
+      tile_pos = Lr / rest;
+      head_ix = full * kHeadGroup + Lr % rest;
+    }
+  }
+  const int bh = head_ix;
   const int ntile = heads_fast ? gridDim.y : gridDim.x;
-  const int tile_ix = heads_fast ? (int)blockIdx.y : (int)blockIdx.x;
+  const int tile_ix = tile_pos;
   const int cta = causal ? (ntile - 1 - tile_ix) : tile_ix;
   const int row0 = cta * (C::QT * C::BM);
   const int nkv = (n + BN - 1) / BN;
