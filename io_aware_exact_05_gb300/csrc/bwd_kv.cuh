@@ -412,11 +412,24 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             uint32_t rr[32];
             tmem_ld32(s_addr + c0, rr);
             tmem_ld_wait();
+            // LSE2 four at a time: one shared-memory wavefront per four words
+            // (every lane reads the same ones); 1.110 -> 1.085 ms on the
+            // B2 H16 n8192 causal backward, with D read the same way
+            {
+              const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float v = ex2(fmaf(__uint_as_float(rr[i]), scale_log2, -lse2[c0 + i]));
-              if (masked && key > qbase + c0 + i) v = 0.f;
-              p[c0 + i] = v;
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 L = l4[i4];
+                p[c0 + 4 * i4] = ex2(fmaf(__uint_as_float(rr[4 * i4]), scale_log2, -L.x));
+                p[c0 + 4 * i4 + 1] = ex2(fmaf(__uint_as_float(rr[4 * i4 + 1]), scale_log2, -L.y));
+                p[c0 + 4 * i4 + 2] = ex2(fmaf(__uint_as_float(rr[4 * i4 + 2]), scale_log2, -L.z));
+                p[c0 + 4 * i4 + 3] = ex2(fmaf(__uint_as_float(rr[4 * i4 + 3]), scale_log2, -L.w));
+              }
+              if (masked) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (key > qbase + c0 + i) p[c0 + i] = 0.f;
+              }
             }
           }
         }
@@ -462,12 +475,17 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               ds[c0 / 2 + 2 * i4] = pack_bf16x2(x0.x, x0.y);
               ds[c0 / 2 + 2 * i4 + 1] = pack_bf16x2(x1.x, x1.y);
             }
-          } else {
+          } else {   // D four at a time
+            const float4* d4 = reinterpret_cast<const float4*>(dd + c0);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              ds[c0 / 2 + i] =
-                  pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd[c0 + 2 * i]),
-                              p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[c0 + 2 * i + 1]));
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 Dq = d4[i4];
+              const int c = c0 + 4 * i4;
+              ds[c / 2] = pack_bf16x2(p[c] * (__uint_as_float(rr[4 * i4]) - Dq.x),
+                                      p[c + 1] * (__uint_as_float(rr[4 * i4 + 1]) - Dq.y));
+              ds[c / 2 + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(rr[4 * i4 + 2]) - Dq.z),
+                                          p[c + 3] * (__uint_as_float(rr[4 * i4 + 3]) - Dq.w));
+            }
           }
         }
         tc_fence_before();
