@@ -87,6 +87,11 @@ struct KvCfgT {
   static constexpr uint32_t ALIGN_SLACK = (BAR_OFF + 256 + 1024 <= 232448) ? 1024 : 0;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + ALIGN_SLACK;
   static constexpr int DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 128;
+  // d = 128: the compute warps read the first 32 LSE2 values of a tile
+  // before waiting for S^T, so that their shared-memory latency stays off
+  // the chain (D cannot follow: P is live by then, and 128 registers do not
+  // hold both)
+  static constexpr bool EARLY_LD = (D == 128);
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the swizzle");
@@ -373,6 +378,11 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
         const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
         ok = mbar_wait(bar(B_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+        float4 pre[C::EARLY_LD ? 8 : 1];   // EARLY_LD: LSE2 of the first 32 columns
+        if constexpr (C::EARLY_LD) {
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) pre[i4] = reinterpret_cast<const float4*>(lse2)[i4];
+        }
         ok = ok && mbar_wait(bar(B_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -411,15 +421,15 @@ bwd_kv128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int c0 = 0; c0 < NC; c0 += 32) {
             uint32_t rr[32];
             tmem_ld32(s_addr + c0, rr);
-            tmem_ld_wait();
             // LSE2 four at a time: one shared-memory wavefront per four words
             // (every lane reads the same ones); 1.110 -> 1.085 ms on the
             // B2 H16 n8192 causal backward, with D read the same way
+            const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
+            tmem_ld_wait();
             {
-              const float4* l4 = reinterpret_cast<const float4*>(lse2 + c0);
 #pragma unroll
               for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 L = l4[i4];
+                const float4 L = (C::EARLY_LD && c0 == 0) ? pre[i4] : l4[i4];
                 p[c0 + 4 * i4] = ex2(fmaf(__uint_as_float(rr[4 * i4]), scale_log2, -L.x));
                 p[c0 + 4 * i4 + 1] = ex2(fmaf(__uint_as_float(rr[4 * i4 + 1]), scale_log2, -L.y));
                 p[c0 + 4 * i4 + 2] = ex2(fmaf(__uint_as_float(rr[4 * i4 + 2]), scale_log2, -L.z));
