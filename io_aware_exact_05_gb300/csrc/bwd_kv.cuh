@@ -32,9 +32,11 @@
 // TMEM and releases the columns; each 64-row half (two warps) then adds its
 // rows into the global fp32 accumulator as four 64 x 32 boxes staged in its
 // own 8 KB of shared memory (128-byte swizzle), one TMA bulk reduce-add
-// each, so two reduce-adds are in flight.  Shared-memory bandwidth, not the
-// tensor pipe, bounds this kernel: the SS products read 128 B/clk while
-// they run, and the tile loads, dS^T stores and dQ staging share the port.
+// each, so two reduce-adds are in flight.  What sets the period at D = 128
+// is the chain through the dP^T columns (dQ(u), its read-out, then
+// dP^T(u+1)) followed by the compute warps' dS and dS^T store; the SS
+// products read 128 B/clk of shared memory while they run and slow down
+// when the tile loads and dQ staging run beside them.
 // Every wait is bounded (mbar_wait).
 #pragma once
 #include <cuda_bf16.h>
