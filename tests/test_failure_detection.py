@@ -3,7 +3,6 @@ nothing completes must end, record ATTN_ERR_DEVICE_TIMEOUT for the host, and
 leave the context usable."""
 
 import pytest
-import torch
 
 import oracle
 from io_aware_exact_05_gb300.inputs import Workload, make_inputs

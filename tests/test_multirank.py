@@ -13,7 +13,6 @@ import subprocess
 import sys
 
 import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
