@@ -138,12 +138,13 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   // head start early instead of the last heads' long tiles trailing the rest
   // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
   // head's K and V shared in L2 by CTAs that run together.
-  // The two CTAs of a key tile (SPLIT_OUT) are neighbours in the grid.
+  // The two CTAs of a key tile (SPLIT_OUT) are neighbours in the grid: the
+  // output index is the fastest part of grid.x, and grid.y stays at most
+  // the head count (the grid's y limit).
   const bool heads_fast = causal || SPARSE;
-  const int kt = heads_fast ? blockIdx.y : blockIdx.x;
-  const int hx = heads_fast ? blockIdx.x : blockIdx.y;
-  const int oh = hx % C::NOUT;                   // SPLIT_OUT: 0 accumulates dV, 1 dK
-  const int bh = hx / C::NOUT;                   // key/value head (K, V, dK, dV)
+  const int kt = heads_fast ? (int)blockIdx.y : (int)blockIdx.x / C::NOUT;
+  const int oh = (int)blockIdx.x % C::NOUT;      // SPLIT_OUT: 0 accumulates dV, 1 dK
+  const int bh = heads_fast ? (int)blockIdx.x / C::NOUT : (int)blockIdx.y;   // key/value head
   const int part = (int)blockIdx.z;              // part of the group (gsplit > 1)
   const bool want_dv = !C::SPLIT_OUT || oh == 0;
   const bool want_dk = !C::SPLIT_OUT || oh == 1;
@@ -819,7 +820,7 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
     return ATTN_ERR_CUDA;
   const int nkt = ceil_div(n, KR);
   dim3 grid = (causal || tl.lists) ? dim3(BHkv * C::NOUT, nkt, gsplit)
-                                   : dim3(nkt, BHkv * C::NOUT, gsplit);
+                                   : dim3(nkt * C::NOUT, BHkv, gsplit);
   kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
