@@ -8,10 +8,13 @@
 // Attention", formulas 1-2).
 //
 // CTA = QT query tiles of 128 rows of one (b, h) head.  Roles:
-//   warp 0 (one lane)  TMA producer: Q tiles once, then K_j and V_j tiles
-//                      into separate shared-memory rings.
-//   warp 1 (one lane)  MMA issuer: S = Q K_j^T (SS-MMA into a TMEM slot),
-//                      O_t += P V_j (TS-MMA: P read from TMEM).
+//   warp 0 (one lane)  TMA producer: Q tiles once, then the K_j tiles into
+//                      their shared-memory ring.
+//   warp 3 (one lane)  TMA producer of the V_j tiles (a ring of their own).
+//   warp 1             MMA issuer (the whole warp runs the loop, an elected
+//                      lane issues): S = Q K_j^T (SS-MMA into a TMEM slot;
+//                      TS with Q in TMEM at d = 256), O_t += P V_j (TS-MMA:
+//                      P read from TMEM).
 //   warp 2             allocates / frees tensor memory; in block-sparse
 //                      launches with two query tiles, warps 1 and 2 each
 //                      issue the MMAs of one tile.
