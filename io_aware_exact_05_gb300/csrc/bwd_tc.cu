@@ -8,30 +8,26 @@
 //   dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
 //   dK = scale dS^T Q,   D_i = dO_i . O_i (from the preprocessing kernel).
 //
-// bwd_kv_kernel -- one CTA per 128-key tile of one head.  Everything is
-// computed transposed so the key index lands on the TMEM lanes:
-//   S^T  = K Q_i^T     (SS-MMA, M = 128 keys, N = BM queries)
-//   dP^T = V dO_i^T    (SS-MMA)
-//   P^T  = 2^(S^T * c - LSE2)       -> bf16 back into TMEM (over S^T)
-//   dV  += P^T dO_i    (TS-MMA: A = P^T from TMEM, B = dO_i MN-major)
-//   dS^T = P^T o (dP^T - D)         -> bf16 into TMEM (over dP^T) and smem
-//   dK  += dS^T Q_i    (TS-MMA)
-//   dQ_i = dS K        (SS-MMA, A = dS MN-major in smem) -> TMEM, then the
-//                      dQ warpgroup adds scale * dQ_i into an fp32
-//                      accumulator in global memory with vector atomics.
-// Only its d = 256 instances are launched (d = 64 and 128 use the pipelined
-// key-tile kernel of bwd_kv.cuh; the dQ-atomic branches here serve no launch
-// now).  For d = 256 the two accumulators would fill the 512 TMEM columns, so
-// two neighbouring CTAs share each key tile: one accumulates all of dV (it
-// needs S^T only: no dP^T, no dS^T, no V), the other all of dK (S^T, dP^T,
-// dS^T), and dQ comes from bwd_q_kernel.  K, the A operand of S^T, sits in
-// the TMEM columns this layout leaves free (S^T is then a TS-MMA), which
-// leaves shared memory for two Q/dO stages.
+// bwd_kv_kernel -- the key-tile kernel at d = 256 (d = 64 and 128 use the
+// pipelined key-tile kernel of bwd_kv.cuh).  dV and dK of a 128-key tile
+// would fill the 512 TMEM columns, so two neighbouring CTAs share each key
+// tile.  Everything is transposed so that the key index lands on the TMEM
+// lanes, and K, the A operand of S^T and constant for the CTA, is copied
+// once into tensor memory (which leaves shared memory for two Q/dO stages):
+//   both CTAs  S^T  = K Q_i^T    (TS-MMA, M = 128 keys, N = 64 queries)
+//              P^T  = 2^(S^T * c - LSE2)
+//   dV CTA     dV  += P^T dO_i   (TS-MMA: P^T in bf16 over S^T)
+//   dK CTA     dP^T = V dO_i^T   (SS-MMA)
+//              dS^T = P^T o (dP^T - D)   -> bf16 over dP^T
+//              dK  += dS^T Q_i   (TS-MMA)
+// In the dQ mode "spill" the dK CTA also stores its dS^T rows into the
+// workspace and dQ = scale dS K is then one GEMM; otherwise dQ comes from
+// bwd_q_kernel.
 //
 // bwd_q_kernel -- one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T,
 // dS = P o (dP - D) -> bf16 TMEM, dQ += dS K_j (TS-MMA); no atomics.  The dQ
-// pass of every head dim (ATTN_DQ_PASS), and the only dQ path at d = 256,
-// where Q sits in TMEM as the A operand of S.
+// pass of every head dim (ATTN_DQ_PASS, and at d = 256 wherever the spill mode
+// does not apply); at d = 256 Q sits in TMEM as the A operand of S.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -57,7 +53,7 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
 }
 
 // ============================================================================ key-tile kernel
-template <int D, bool DQ>
+template <int D>
 struct KvCfg {
   static constexpr int BNK = 128;                    // keys per CTA (TMEM lanes)
   static constexpr int BM = (D == 256) ? 64 : 128;   // queries per iteration
@@ -71,8 +67,6 @@ struct KvCfg {
   // d = 256: K (the A operand of S^T = K Q^T, constant for the CTA) lives in
   // tensor memory, which frees the shared memory of a second Q/dO stage
   static constexpr bool K_IN_TMEM = (D == 256);
-  static constexpr bool WITH_DQ = DQ;                // atomic dQ shares from this kernel
-  static constexpr bool DS_ALIAS = DQ && D == 128;   // dS reuses the dO stage buffer
   static constexpr int NKB = D / 64;
   static constexpr uint32_t KV_BYTES = BNK * D * 2;
   static constexpr uint32_t QT_BYTES = BM * D * 2;   // one Q or dO tile
@@ -83,9 +77,7 @@ struct KvCfg {
   static constexpr uint32_t ST_OFF = K_IN_TMEM ? KV_BYTES : 2 * KV_BYTES;
   // where K's load lands: the second stage, before that stage's first use
   static constexpr uint32_t K_LOAD_OFF = K_IN_TMEM ? ST_OFF + STAGE : K_OFF;
-  static constexpr uint32_t DS_OFF = ST_OFF + STG * STAGE;  // dedicated dS buffer (D = 64)
-  static constexpr uint32_t DS_BYTES = (WITH_DQ && !DS_ALIAS) ? BM * BNK * 2 : 0;
-  static constexpr uint32_t BAR_OFF = DS_OFF + DS_BYTES;
+  static constexpr uint32_t BAR_OFF = ST_OFF + STG * STAGE;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
   // TMEM columns (SPLIT_OUT: the CTA's one accumulator at column 0)
   static constexpr int DV_COL = 0;
@@ -93,16 +85,15 @@ struct KvCfg {
   static constexpr int S_COL = SPLIT_OUT ? DO : 2 * DO;
   static constexpr int DP_COL = S_COL + BM;
   static constexpr int K_COL = S_COL + 2 * BM;        // K as A operand (K_IN_TMEM)
-  static constexpr int NTHREADS = WITH_DQ ? 512 : 384;
+  static constexpr int NTHREADS = 384;
+  static_assert(D == 256, "head dims 64 and 128 use the key-tile kernel of bwd_kv.cuh");
   static_assert(S_COL + 2 * BM + (K_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
-  static_assert(!K_IN_TMEM || (KV_BYTES <= STAGE && !DQ), "K in tensor memory: no dQ here");
-  static_assert(!WITH_DQ || (BM == 128 && D <= BM), "dQ tile reuses the S columns");
-  static_assert(!(D == 256 && DQ), "d = 256 takes dQ from the query-tile kernel");
+  static_assert(!K_IN_TMEM || KV_BYTES <= STAGE, "K's load lands in the second stage");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8, K_DVD = 9,
-             K_DQF = 10, K_DQE = 11, K_ACC = 12, K_DRAIN = 13, K_CP = 14 };
+enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8,
+             K_ACC = 12, K_DRAIN = 13, K_CP = 14 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
 // one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
@@ -111,18 +102,18 @@ enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR 
 // tile, key tiles start KR keys apart, and the other keys' probabilities are
 // set to 0 (less K and V kept on chip, Q and dO streamed 128 / KR times as
 // often).
-template <int D, bool DQ, bool GROUPED, bool SPARSE, int KR = 128>
-__global__ void __launch_bounds__(KvCfg<D, DQ>::NTHREADS, 1)
+template <int D, bool GROUPED, bool SPARSE, int KR = 128>
+__global__ void __launch_bounds__(KvCfg<D>::NTHREADS, 1)
 bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ LSE2, const float* __restrict__ Dv,
-              float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dK,
+              __nv_bfloat16* __restrict__ dK,
               __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
               float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n, int n_pad,
               float scale, float scale_log2, int causal, KernelCtl ctl,
               __nv_bfloat16* __restrict__ dSt, int ld_ds) {
-  using C = KvCfg<D, DQ>;
-  static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED && !DQ),
+  using C = KvCfg<D>;
+  static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED),
                 "owned key rows: a dense, one-head-per-head study instance");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -173,9 +164,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(K_DPF), 1);
     mbar_init(bar(K_PR), 256);
     mbar_init(bar(K_DSR), 256);
-    mbar_init(bar(K_DVD), 1);
-    mbar_init(bar(K_DQF), 1);
-    mbar_init(bar(K_DQE), 128);
     mbar_init(bar(K_ACC), 1);
     mbar_init(bar(K_DRAIN), 1);
     mbar_init(bar(K_CP), 128);
@@ -244,7 +232,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       // (the whole warp runs the loop; one elected lane issues each MMA/commit)
       constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V K-major, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
-      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);        // dS MN-major, K MN-major
       bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (C::K_IN_TMEM) ok = ok && mbar_wait_warp(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV);
       const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
@@ -253,9 +240,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
         const uint32_t qa = st, ga = st + C::QT_BYTES;
         if (!(ok = mbar_wait_warp(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
-        if (C::WITH_DQ && u > 0) {
-          if (!(ok = mbar_wait_warp(bar(K_DQE), (u - 1) & 1, abort_flag, ctl, SITE_BWD_DQ_FREE))) break;
-        }
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T  (contraction over d, 16 per instruction)
 #pragma unroll
@@ -292,9 +276,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
                    sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
           }
-          if (C::DS_ALIAS) tc_commit(bar(K_DVD));
         }
-        // dK += dS^T Q ; dQ_i = dS K
+        // dK += dS^T Q
         if (want_dk) {
           if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
           tc_fence_after();
@@ -306,14 +289,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                    sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
           }
         }
-        if (C::WITH_DQ) {
-          const uint32_t dsa = C::DS_ALIAS ? ga : (sb + C::DS_OFF);
-#pragma unroll
-          for (int kk = 0; kk < C::BNK / 16; ++kk)
-            mma_ss(tmem + C::S_COL, sdesc_sw128(dsa + kk * 2048, C::BNK * 128, 1024),
-                   sdesc_sw128(ka + kk * 2048, C::BNK * 128, 1024), id_dq, kk > 0);
-          tc_commit(bar(K_DQF));
-        }
         tc_commit(bar(K_QE + s));
       }
       tc_commit(bar(K_ACC));
@@ -324,7 +299,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
     }
     __syncwarp();
-  } else if (warp < 12) {
+  } else {
     // ---------------------------------------------------------------- compute
     const int q = warp & 3, h = (warp - 4) >> 2;
     const int r = q * 32 + lane;          // key row within the tile (TMEM lane)
@@ -427,21 +402,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
         }
         tmem_st_wait();
-        if (C::WITH_DQ) {
-          if (C::DS_ALIAS) {
-            ok = mbar_wait(bar(K_DVD), u & 1, abort_flag, ctl, SITE_BWD_DS_FREE);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          }
-          // dS as the MN-major A operand of dQ = dS K: query block h (64 queries)
-          // is one 128-byte row per key, eight 16-byte chunks, 128-byte swizzle.
-          uint8_t* dsb = C::DS_ALIAS ? const_cast<uint8_t*>(stp) + C::QT_BYTES : smem + C::DS_OFF;
-          uint8_t* rowp = dsb + h * (C::BNK * 128);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(rowp + sw128_offset(r, c)) =
-                make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
-          fence_proxy_async_smem();
-        }
         tc_fence_before();
         mbar_arrive(bar(K_DSR));
       }
@@ -479,47 +439,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                          mul * __uint_as_float(rr[i + 3]));
           } else {
             store32_bf16((out_dv ? dV : dK) + off + c0, rr, mul);
-          }
-        }
-      }
-    }
-  } else {
-    // ---------------------------------------------------------------- dQ epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;     // query row within the tile
-    const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + C::S_COL;
-    bool go = true;
-    for (int gi = 0, u = 0; go && gi < gper; ++gi) {
-      const int bq = qbase + gi;
-      for (int ut = 0; ut < cnt; ++ut, ++u) {
-        bool ok = mbar_wait(bar(K_DQF), u & 1, abort_flag, ctl, SITE_BWD_DQ_FULL);
-        if (!__all_sync(0xffffffffu, ok)) {
-          go = false;
-          break;
-        }
-        tc_fence_after();
-        const int qrow = qtile(ut) * C::BM + r;
-        float* dst = dQacc + ((size_t)bq * n + qrow) * D;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t a[32], b[32];
-          tmem_ld32(src + c0, a);
-          tmem_ld32(src + c0 + 32, b);
-          tmem_ld_wait();
-          if (c0 + 64 >= D) {   // all of dQ_i is in registers: release the columns
-            tc_fence_before();
-            mbar_arrive(bar(K_DQE));
-          }
-          if (qrow < n) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              red_add_v4(dst + c0 + i, scale * __uint_as_float(a[i]), scale * __uint_as_float(a[i + 1]),
-                         scale * __uint_as_float(a[i + 2]), scale * __uint_as_float(a[i + 3]));
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              red_add_v4(dst + c0 + 32 + i, scale * __uint_as_float(b[i]),
-                         scale * __uint_as_float(b[i + 1]), scale * __uint_as_float(b[i + 2]),
-                         scale * __uint_as_float(b[i + 3]));
           }
         }
       }
@@ -794,13 +713,13 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   if (warp == 2) tmem_dealloc<512>(tmem);
 }
 
-template <int D, bool DQ, int KR = 128>
+template <int D, int KR = 128>
 int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, const float* LSE2,
-                  const float* Dv, float* dQacc, void* dK, void* dV, float* dKacc, float* dVacc,
+                  const float* Dv, void* dK, void* dV, float* dKacc, float* dVacc,
                   int BH, const HeadMap& hm, int gsplit, const TileLists& tl, int n, int n_pad,
                   float scale, int causal, const KernelCtl& ctl, cudaStream_t st,
                   void* dSt = nullptr, int ld_ds = 0) {
-  using C = KvCfg<D, DQ>;
+  using C = KvCfg<D>;
   const int BHkv = BH / hm.group;
   CUtensorMap tq, tk, tv, tg;
   if (!make_tmap_bf16(&tq, Q, D, n, BH, 64, C::BM) ||
@@ -809,10 +728,10 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
       !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
   if (tl.lists && hm.group > 1) return ATTN_ERR_UNSUPPORTED;
-  auto kern = bwd_kv_kernel<D, DQ, false, false, KR>;
+  auto kern = bwd_kv_kernel<D, false, false, KR>;
   if constexpr (KR == C::BNK) {
-    if (tl.lists) kern = bwd_kv_kernel<D, DQ, false, true>;
-    else if (hm.group > 1) kern = bwd_kv_kernel<D, DQ, true, false>;
+    if (tl.lists) kern = bwd_kv_kernel<D, false, true>;
+    else if (hm.group > 1) kern = bwd_kv_kernel<D, true, false>;
   } else if (tl.lists || hm.group > 1) {
     return ATTN_ERR_UNSUPPORTED;
   }
@@ -821,7 +740,7 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
   const int nkt = ceil_div(n, KR);
   dim3 grid = (causal || tl.lists) ? dim3(BHkv * C::NOUT, nkt, gsplit)
                                    : dim3(nkt * C::NOUT, BHkv, gsplit);
-  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv, dQacc,
+  kern<<<grid, C::NTHREADS, C::SMEM, st>>>(tq, tk, tv, tg, LSE2, Dv,
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
                                            gsplit, tl, n, n_pad, scale,
@@ -867,9 +786,6 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
   if (dSt && (d != 256 || hm.group != 1 || tl.lists || causal || ld_ds < n || ld_ds % 8 ||
               (reinterpret_cast<uintptr_t>(dSt) & 15u)))
     return ATTN_ERR_UNSUPPORTED;
-#define ATTN_KV(DD, DQQ)                                                                      \
-  return launch_kv_cfg<DD, DQQ>(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm,    \
-                                gsplit, tl, n, n_pad, scale, causal, ctl, st, dSt, ld_ds)
   const bool dq = dQacc != nullptr;
   switch (d) {
     case 64:
@@ -878,10 +794,12 @@ int launch_bwd_kv_tc(const void* Q, const void* K, const void* V, const void* dO
     case 128:
       return launch_bwd_kv128_tc(Q, K, V, dO, LSE2, Dv, dQacc, dK, dV, dKacc, dVacc, BH, hm, gsplit,
                                  tl, n, n_pad, scale, causal, ctl, st);
-    case 256: if (dq) return ATTN_ERR_UNSUPPORTED; ATTN_KV(256, false);
+    case 256:   // dQ from the query-tile pass or the spill GEMM, never from this kernel
+      if (dq) return ATTN_ERR_UNSUPPORTED;
+      return launch_kv_cfg<256>(Q, K, V, dO, LSE2, Dv, dK, dV, dKacc, dVacc, BH, hm, gsplit, tl, n,
+                                n_pad, scale, causal, ctl, st, dSt, ld_ds);
     default: return ATTN_ERR_UNSUPPORTED;
   }
-#undef ATTN_KV
 }
 
 int launch_bwd_kv_study(const void* Q, const void* K, const void* V, const void* dO,
@@ -894,7 +812,7 @@ int launch_bwd_kv_study(const void* Q, const void* K, const void* V, const void*
                                        n_pad, d, scale, causal, ctl, st);
   if (dQacc) return ATTN_ERR_UNSUPPORTED;
 #define ATTN_KVS(KRR)                                                                          \
-  return launch_kv_cfg<256, false, KRR>(Q, K, V, dO, LSE2, Dv, nullptr, dK, dV, nullptr, nullptr, \
+  return launch_kv_cfg<256, KRR>(Q, K, V, dO, LSE2, Dv, dK, dV, nullptr, nullptr,               \
                                         BH, hm, 1, TileLists(), n, n_pad, scale, causal, ctl, st)
   switch (key_rows) {
     case 128: ATTN_KVS(128);
