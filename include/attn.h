@@ -80,7 +80,7 @@ typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, size < 1, bad scale */
   ATTN_ERR_UNSUPPORTED = 2,   /* head dim not supported for this dtype/path */
-  ATTN_ERR_WORKSPACE = 3,     /* workspace null or smaller than required */
+  ATTN_ERR_WORKSPACE = 3,     /* workspace null, not 256-byte aligned or too small */
   ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
   ATTN_ERR_DEVICE_TIMEOUT = 5 /* a bounded device-side wait ran out */
 } attn_status_t;

@@ -1,6 +1,7 @@
-"""Parity at sequence lengths beyond the workloads' (n = 131072 at d = 64 and
-128, n = 65536 at d = 256, causal), through the default API calls: row
-offsets near 2^17 in every kernel, 1024 key tiles in a causal grid, and (at
+"""Parity at sequence lengths beyond the workloads' (n = 131072 and 2^20 at
+d = 64 and 128, n = 65536 at d = 256, causal), through the default API
+calls: row offsets up to 2^20 in every kernel, up to 8192 key tiles in a
+causal grid, and (at
 d = 256) the automatic dQ mode falling back to the query-tile pass because
 the n x n dS^T buffer would exceed 4 GiB.
 
@@ -25,6 +26,8 @@ CASES = [
     Workload("long_n128k_d64", 1, 2, 131072, 64, "bf16", True, 1.0, 2910),
     Workload("long_n128k_d128", 1, 2, 131072, 128, "bf16", True, 1.0, 2920),
     Workload("long_n64k_d256", 1, 1, 65536, 256, "bf16", True, 1.0, 2930),
+    Workload("long_n1m_d64", 1, 1, 1 << 20, 64, "bf16", True, 1.0, 2950),
+    Workload("long_n1m_d128", 1, 1, 1 << 20, 128, "bf16", True, 1.0, 2960),
 ]
 
 
