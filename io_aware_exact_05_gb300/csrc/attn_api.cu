@@ -35,7 +35,7 @@ bool bf16_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 constexpr size_t kSpillAutoMaxBytes = size_t(4) << 30;
 
 // dQ mode actually used for a bf16 shape (measured choices).  d <= 128: the
-// key-tile kernel's reduce-adds (1.25-1.48 x faster than the pass).  d = 256:
+// key-tile kernel's reduce-adds (1.29-1.48 x faster than the pass).  d = 256:
 // the key-tile kernel has no tensor-memory columns for a dQ tile; the spill
 // mode (dS^T through the workspace, one GEMM) is 17 % faster than the pass
 // where it applies (non-causal, dense, one key/value head per query head)
