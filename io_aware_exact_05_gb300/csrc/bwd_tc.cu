@@ -13,13 +13,19 @@
 // would fill the 512 TMEM columns, so two neighbouring CTAs share each key
 // tile.  Everything is transposed so that the key index lands on the TMEM
 // lanes, and K, the A operand of S^T and constant for the CTA, is copied
-// once into tensor memory (which leaves shared memory for two Q/dO stages):
+// once into tensor memory (which leaves shared memory for three Q and two
+// dO slots):
 //   both CTAs  S^T  = K Q_i^T    (TS-MMA, M = 128 keys, N = 64 queries)
 //              P^T  = 2^(S^T * c - LSE2)
 //   dV CTA     dV  += P^T dO_i   (TS-MMA: P^T in bf16 over S^T)
 //   dK CTA     dP^T = V dO_i^T   (SS-MMA)
 //              dS^T = P^T o (dP^T - D)   -> bf16 over dP^T
 //              dK  += dS^T Q_i   (TS-MMA)
+// Neither CTA lets its tensor pipe wait for the compute warps of a tile:
+// the dV CTA, which has no dP^T, alternates S^T between two column slots and
+// issues S^T(i+1) before dV(i); the dK CTA issues S^T(i+1) as soon as its
+// compute warps hold P(i) in registers, so the pipe runs dP^T(i), S^T(i+1),
+// dK(i) back to back while they form dS^T(i).
 // In the dQ mode "spill" the dK CTA also stores its dS^T rows into the
 // workspace and dQ = scale dS K is then one GEMM; otherwise dQ comes from
 // bwd_q_kernel.
@@ -29,6 +35,8 @@
 // pass of every head dim (ATTN_DQ_PASS, and at d = 256 wherever the spill mode
 // does not apply); at d = 256 Q sits in TMEM as the A operand of S.
 #include <cuda_bf16.h>
+
+#include <cstring>
 
 #include "kernels.h"
 #include "sm100.cuh"
@@ -56,44 +64,53 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
 template <int D>
 struct KvCfg {
   static constexpr int BNK = 128;                    // keys per CTA (TMEM lanes)
-  static constexpr int BM = (D == 256) ? 64 : 128;   // queries per iteration
+  static constexpr int BM = 64;                      // queries per iteration
   static constexpr int DO = D;                       // accumulator columns (all of d)
-  // d = 256: dV and dK of a key tile would take all 512 TMEM columns, so two
-  // CTAs share a key tile, one accumulating dV (needs S only) and one dK
-  // (needs S and dP); each recomputes S, only the dK CTA computes dP
-  static constexpr bool SPLIT_OUT = (D == 256);
-  static constexpr int NOUT = SPLIT_OUT ? 2 : 1;     // CTAs per key tile
-  static constexpr int STG = 2;
-  // d = 256: K (the A operand of S^T = K Q^T, constant for the CTA) lives in
-  // tensor memory, which frees the shared memory of a second Q/dO stage
-  static constexpr bool K_IN_TMEM = (D == 256);
+  // dV and dK of a key tile would take all 512 TMEM columns, so two CTAs
+  // share a key tile, one accumulating dV (needs S only) and one dK (needs S
+  // and dP); each recomputes S, only the dK CTA computes dP
+  static constexpr int NOUT = 2;                     // CTAs per key tile
+  // Q and dO tiles in separate rings, each slot released by its last reader:
+  // the dK CTA reads Q(i) until dK(i) and dO(i) until dP^T(i), the dV CTA
+  // Q(i) until S^T(i) and dO(i) until dV(i).  Three Q slots give the load of
+  // Q(i+1) a whole iteration in the dK CTA, where S^T(i+1) runs before dK(i).
+  static constexpr int QSL = 3;
+  static constexpr int OSL = 2;
   static constexpr int NKB = D / 64;
   static constexpr uint32_t KV_BYTES = BNK * D * 2;
   static constexpr uint32_t QT_BYTES = BM * D * 2;   // one Q or dO tile
   static constexpr uint32_t STAT_BYTES = BM * 4;     // LSE2 or D of the tile
-  static constexpr uint32_t STAGE = 2 * QT_BYTES + 1024;   // Q, dO, LSE2 + D (padded)
-  static constexpr uint32_t K_OFF = 0;                              // unused when K_IN_TMEM
-  static constexpr uint32_t V_OFF = K_IN_TMEM ? 0 : KV_BYTES;
-  static constexpr uint32_t ST_OFF = K_IN_TMEM ? KV_BYTES : 2 * KV_BYTES;
-  // where K's load lands: the second stage, before that stage's first use
-  static constexpr uint32_t K_LOAD_OFF = K_IN_TMEM ? ST_OFF + STAGE : K_OFF;
-  static constexpr uint32_t BAR_OFF = ST_OFF + STG * STAGE;
-  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
-  // TMEM columns (SPLIT_OUT: the CTA's one accumulator at column 0)
-  static constexpr int DV_COL = 0;
-  static constexpr int DK_COL = SPLIT_OUT ? 0 : DO;
-  static constexpr int S_COL = SPLIT_OUT ? DO : 2 * DO;
+  static constexpr uint32_t V_OFF = 0;
+  static constexpr uint32_t QS_OFF = KV_BYTES;                       // Q slots
+  static constexpr uint32_t OS_OFF = QS_OFF + QSL * QT_BYTES;        // dO slots
+  // the row statistics travel with the slot their last reader releases:
+  // LSE2 and D with Q in the dK CTA, LSE2 with dO in the dV CTA
+  static constexpr uint32_t QST_OFF = OS_OFF + OSL * QT_BYTES;
+  static constexpr uint32_t OST_OFF = QST_OFF + QSL * 2 * STAT_BYTES;
+  static constexpr uint32_t BAR_OFF = OST_OFF + OSL * STAT_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + 256;    // base must be 1024-byte aligned
+  // K (the A operand of S^T = K Q^T, constant for the CTA) is copied into
+  // tensor memory; its load lands in Q slots 1 and 2 of the dK CTA (which
+  // holds V) and in the unused V area of the dV CTA
+  static constexpr uint32_t K_LOAD_DK = QS_OFF + QT_BYTES;
+  // TMEM columns: the CTA's one accumulator, S^T, dP^T (the dV CTA's second
+  // S^T slot), K
+  static constexpr int ACC_COL = 0;
+  static constexpr int S_COL = DO;
   static constexpr int DP_COL = S_COL + BM;
-  static constexpr int K_COL = S_COL + 2 * BM;        // K as A operand (K_IN_TMEM)
+  static constexpr int K_COL = S_COL + 2 * BM;
   static constexpr int NTHREADS = 384;
   static_assert(D == 256, "head dims 64 and 128 use the key-tile kernel of bwd_kv.cuh");
-  static_assert(S_COL + 2 * BM + (K_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
-  static_assert(!K_IN_TMEM || KV_BYTES <= STAGE, "K's load lands in the second stage");
+  static_assert(K_COL + D / 2 <= 512, "tensor memory budget");
+  static_assert(2 * QT_BYTES == KV_BYTES, "K's load fills Q slots 1 and 2");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum : int { K_KV = 0, K_QF = 1, K_QE = 3, K_SF = 5, K_DPF = 6, K_PR = 7, K_DSR = 8,
-             K_ACC = 12, K_DRAIN = 13, K_CP = 14 };
+// K_DSS (dQ mode "spill", one per dO slot): the compute warps have staged
+// dS^T of the tile in that slot for the TMA store.
+enum : int { K_KV = 0, K_QF = 1, K_QE = 4, K_OF = 7, K_OE = 9, K_SF = 11, K_SF1 = 12, K_DPF = 13,
+             K_PR = 14, K_PR1 = 15, K_SC = 16, K_DSR = 17, K_ACC = 18, K_DRAIN = 19, K_CP = 20,
+             K_DSS = 21 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
 // one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
@@ -111,12 +128,19 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               __nv_bfloat16* __restrict__ dV, float* __restrict__ dKacc,
               float* __restrict__ dVacc, HeadMap hm, int gsplit, TileLists tl, int n, int n_pad,
               float scale, float scale_log2, int causal, KernelCtl ctl,
-              __nv_bfloat16* __restrict__ dSt, int ld_ds) {
+              const __grid_constant__ CUtensorMap tmS, int spill_ds) {
   using C = KvCfg<D>;
   static_assert(KR == C::BNK || (KR >= 32 && KR < C::BNK && !SPARSE && !GROUPED),
                 "owned key rows: a dense, one-head-per-head study instance");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1k(smem_raw);
+  // the layout has no room to align itself: it needs the base 1024-byte
+  // aligned (the 128-byte swizzle atoms); report and leave before touching
+  // anything
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(ctl, ATTN_ERR_CUDA, SITE_BWD_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -129,16 +153,15 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   // head start early instead of the last heads' long tiles trailing the rest
   // (CTAs start in grid order).  Otherwise tiles vary fastest, which keeps a
   // head's K and V shared in L2 by CTAs that run together.
-  // The two CTAs of a key tile (SPLIT_OUT) are neighbours in the grid: the
-  // output index is the fastest part of grid.x, and grid.y stays at most
-  // the head count (the grid's y limit).
+  // The two CTAs of a key tile are neighbours in the grid: the output index
+  // is the fastest part of grid.x, and grid.y stays at most the head count
+  // (the grid's y limit).
   const bool heads_fast = causal || SPARSE;
   const int kt = heads_fast ? (int)blockIdx.y : (int)blockIdx.x / C::NOUT;
-  const int oh = (int)blockIdx.x % C::NOUT;      // SPLIT_OUT: 0 accumulates dV, 1 dK
+  const int oh = (int)blockIdx.x % C::NOUT;      // 0 accumulates dV, 1 dK
   const int bh = heads_fast ? (int)blockIdx.x / C::NOUT : (int)blockIdx.y;   // key/value head
   const int part = (int)blockIdx.z;              // part of the group (gsplit > 1)
-  const bool want_dv = !C::SPLIT_OUT || oh == 0;
-  const bool want_dk = !C::SPLIT_OUT || oh == 1;
+  const bool want_dk = oh == 1, want_dv = !want_dk;
   const int k0 = kt * KR;
   const int nq = (n + C::BM - 1) / C::BM;
   const int i_start = causal ? (k0 / C::BM) : 0;
@@ -153,16 +176,38 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int gper = GROUPED ? hm.group / gsplit : 1;
   const int qbase = GROUPED ? hm.q_of(bh, part * gper) : bh;
   const int total = gper * cnt;
+  const uint32_t k_load = want_dk ? C::K_LOAD_DK : C::V_OFF;
+  // dQ mode "spill": the dK CTA also writes dS^T ([BH][n keys][n queries]
+  // through tmS) for dQ = scale dS K as one GEMM.  Its compute warps stage
+  // each tile's dS^T in the dO slot that dP^T has just consumed, and warp 3
+  // stores it with TMA and then releases the slot.
+  const bool spill = !GROUPED && !SPARSE && KR == C::BNK && spill_ds != 0 && want_dk;
+  // S^T of iteration u, its columns and its barriers.  The dK CTA keeps one
+  // slot (its dP^T columns receive dS^T); the dV CTA has no dP^T, so its S^T
+  // alternates between the S^T and the dP^T columns, with a "full" and a
+  // "P ready" barrier per slot (each waited with the parity of u / 2).
+  auto s_col = [&](int u) { return (want_dk || !(u & 1)) ? C::S_COL : C::DP_COL; };
+  auto sf_bar = [&](int u) { return (want_dk || !(u & 1)) ? bar(K_SF) : bar(K_SF1); };
+  auto sf_par = [&](int u) { return want_dk ? (u & 1) : ((u >> 1) & 1); };
+  auto pr_bar = [&](int u) { return (u & 1) ? bar(K_PR1) : bar(K_PR); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(K_KV), 1);
-    for (int s = 0; s < C::STG; ++s) {
+    for (int s = 0; s < C::QSL; ++s) {
       mbar_init(bar(K_QF + s), 1);
       mbar_init(bar(K_QE + s), 1);
     }
+    for (int s = 0; s < C::OSL; ++s) {
+      mbar_init(bar(K_OF + s), 1);
+      mbar_init(bar(K_OE + s), 1);
+      mbar_init(bar(K_DSS + s), 256);
+    }
     mbar_init(bar(K_SF), 1);
+    mbar_init(bar(K_SF1), 1);
     mbar_init(bar(K_DPF), 1);
     mbar_init(bar(K_PR), 256);
+    mbar_init(bar(K_PR1), 256);
+    mbar_init(bar(K_SC), 256);
     mbar_init(bar(K_DSR), 256);
     mbar_init(bar(K_ACC), 1);
     mbar_init(bar(K_DRAIN), 1);
@@ -173,6 +218,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    if (spill) tma_prefetch_desc(&tmS);
   }
   if (warp == 2) tmem_alloc<512>(smem_u32(tmem_slot));
   tc_fence_before();
@@ -182,50 +228,98 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (warp < 4) {
     if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------------------------ K, V and Q producer
       mbar_expect_tx(bar(K_KV), (want_dk ? 2 : 1) * C::KV_BYTES);   // V only for dP
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
-        tma_load_3d(sb + C::K_LOAD_OFF + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
+        tma_load_3d(sb + k_load + kb * (C::BNK * 128), &tmK, kb * 64, k0, bh, bar(K_KV));
         if (want_dk)
           tma_load_3d(sb + C::V_OFF + kb * (C::BNK * 128), &tmV, kb * 64, k0, bh, bar(K_KV));
       }
-      int issued_last[2] = {-1, -1};
+      // Q (with LSE2 and D in the dK CTA); dO has its own producer (warp 2)
+      int q_last[C::QSL];
+      for (int s = 0; s < C::QSL; ++s) q_last[s] = -1;
       bool go = true;
       for (int gi = 0, u = 0; go && gi < gper; ++gi) {
         const int bq = qbase + gi;
         for (int ut = 0; ut < cnt; ++ut, ++u) {
-          const int s = u % C::STG;
+          const int qs = u % C::QSL;
           const int q0 = qtile(ut) * C::BM;
-          if (!mbar_wait(bar(K_QE + s), ((u / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+          if (!mbar_wait(bar(K_QE + qs), ((u / C::QSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
             go = false;
             break;
           }
-          // the second stage holds K until it has been copied to tensor memory
-          if (C::K_IN_TMEM && u == 1 &&
-              !mbar_wait(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV)) {
+          // Q slots 1 and 2 of the dK CTA hold K until it has been copied to tensor memory
+          if (want_dk && u == 1 && !mbar_wait(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV)) {
             go = false;
             break;
           }
-          const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
-          mbar_expect_tx(bar(K_QF + s), 2 * C::QT_BYTES + 2 * C::STAT_BYTES);
+          const uint32_t qd = sb + C::QS_OFF + qs * C::QT_BYTES;
+          mbar_expect_tx(bar(K_QF + qs), C::QT_BYTES + (want_dk ? 2 * C::STAT_BYTES : 0));
 #pragma unroll
-          for (int kb = 0; kb < C::NKB; ++kb) {
-            tma_load_3d(st + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(K_QF + s));
-            tma_load_3d(st + C::QT_BYTES + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(K_QF + s));
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_3d(qd + kb * (C::BM * 128), &tmQ, kb * 64, q0, bq, bar(K_QF + qs));
+          if (want_dk) {
+            const uint32_t stq = sb + C::QST_OFF + qs * 2 * C::STAT_BYTES;
+            bulk_load(stq, LSE2 + (size_t)bq * n_pad + q0, C::STAT_BYTES, bar(K_QF + qs));
+            bulk_load(stq + C::STAT_BYTES, Dv + (size_t)bq * n_pad + q0, C::STAT_BYTES,
+                      bar(K_QF + qs));
           }
-          bulk_load(st + 2 * C::QT_BYTES, LSE2 + (size_t)bq * n_pad + q0, C::STAT_BYTES, bar(K_QF + s));
-          bulk_load(st + 2 * C::QT_BYTES + 512, Dv + (size_t)bq * n_pad + q0, C::STAT_BYTES,
-                    bar(K_QF + s));
-          issued_last[s] = u;
+          q_last[qs] = u;
         }
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         mbar_wait(bar(K_KV), 0, &no_abort, ctl, SITE_BWD_KV);
-        for (int s = 0; s < C::STG; ++s)
-          if (issued_last[s] >= 0)
-            mbar_wait(bar(K_QF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+        for (int s = 0; s < C::QSL; ++s)
+          if (q_last[s] >= 0)
+            mbar_wait(bar(K_QF + s), (q_last[s] / C::QSL) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+      }
+    } else if (warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ dO producer
+      // (with LSE2 in the dV CTA)
+      int o_last[C::OSL];
+      for (int s = 0; s < C::OSL; ++s) o_last[s] = -1;
+      bool go = true;
+      for (int gi = 0, u = 0; go && gi < gper; ++gi) {
+        const int bq = qbase + gi;
+        for (int ut = 0; ut < cnt; ++ut, ++u) {
+          const int os = u % C::OSL;
+          const int q0 = qtile(ut) * C::BM;
+          if (!mbar_wait(bar(K_OE + os), ((u / C::OSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+            go = false;
+            break;
+          }
+          const uint32_t od = sb + C::OS_OFF + os * C::QT_BYTES;
+          mbar_expect_tx(bar(K_OF + os), C::QT_BYTES + (want_dv ? C::STAT_BYTES : 0));
+#pragma unroll
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_3d(od + kb * (C::BM * 128), &tmdO, kb * 64, q0, bq, bar(K_OF + os));
+          if (want_dv)
+            bulk_load(sb + C::OST_OFF + os * C::STAT_BYTES, LSE2 + (size_t)bq * n_pad + q0,
+                      C::STAT_BYTES, bar(K_OF + os));
+          o_last[os] = u;
+        }
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < C::OSL; ++s)
+          if (o_last[s] >= 0)
+            mbar_wait(bar(K_OF + s), (o_last[s] / C::OSL) & 1, &no_abort, ctl, SITE_BWD_Q_FULL);
+      }
+    } else if (warp == 3 && lane == 0) {
+      // ------------------------------------------------------------ dS^T store (spill)
+      if (spill) {
+        for (int u = 0; u < total; ++u) {   // one query head (no group, no tile list)
+          const int os = u % C::OSL;
+          if (!mbar_wait(bar(K_DSS + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_DS_READY))
+            break;
+          tma_store_3d(&tmS, sb + C::OS_OFF + os * C::QT_BYTES, qtile(u) * C::BM, k0, bh);
+          bulk_commit_group();
+          bulk_wait_read_all();   // the slot has been read: dO(u + 2) may load
+          mbar_arrive(bar(K_OE + os));
+        }
+        bulk_wait_all();
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
@@ -233,28 +327,43 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t id_s = idesc_bf16(128, C::BM, false, false);   // K/V K-major, Q/dO K-major
       constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
       bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
-      if (C::K_IN_TMEM) ok = ok && mbar_wait_warp(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV);
-      const uint32_t ka = sb + C::K_OFF, va = sb + C::V_OFF;
-      for (int u = 0; ok && u < total; ++u) {
-        const int s = u % C::STG;
-        const uint32_t st = sb + C::ST_OFF + s * C::STAGE;
-        const uint32_t qa = st, ga = st + C::QT_BYTES;
-        if (!(ok = mbar_wait_warp(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
-        tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T  (contraction over d, 16 per instruction)
+      ok = ok && mbar_wait_warp(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV);
+      const uint32_t va = sb + C::V_OFF;
+      // S^T(u) = K Q_u^T into column col: A = K from tensor memory (16
+      // elements = 8 columns per MMA), contraction over d
+      auto issue_s = [&](int u, int col) {
+        const uint32_t qa = sb + C::QS_OFF + (u % C::QSL) * C::QT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          if (C::K_IN_TMEM)   // A = K from tensor memory, 16 elements = 8 columns per MMA
-            mma_ts(tmem + C::S_COL, tmem + C::K_COL + 8 * kk, sdesc_sw128(qa + qoff, 16, 1024),
-                   id_s, kk > 0);
-          else
-            mma_ss(tmem + C::S_COL, sdesc_sw128(ka + koff, 16, 1024),
-                   sdesc_sw128(qa + qoff, 16, 1024), id_s, kk > 0);
+          mma_ts(tmem + col, tmem + C::K_COL + 8 * kk, sdesc_sw128(qa + qoff, 16, 1024), id_s,
+                 kk > 0);
         }
-        tc_commit(bar(K_SF));
+      };
+      // S^T of the next tile is issued before this tile's accumulator
+      // product: in the dV CTA into the other slot, in the dK CTA as soon as
+      // the compute warps hold P in registers (K_SC), so that it runs while
+      // they form dS^T.
+      if (ok && total > 0) {
+        ok = mbar_wait_warp(bar(K_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, s_col(0));
+          tc_commit(sf_bar(0));
+          if (want_dv) tc_commit(bar(K_QE));   // the dV CTA reads Q only in S^T
+        }
+      }
+      for (int u = 0; ok && u < total; ++u) {
+        const int qs = u % C::QSL, os = u % C::OSL;
+        const int qn = (u + 1) % C::QSL, pn = ((u + 1) / C::QSL) & 1;
+        const bool more = u + 1 < total;
+        const uint32_t qa = sb + C::QS_OFF + qs * C::QT_BYTES;
+        const uint32_t ga = sb + C::OS_OFF + os * C::QT_BYTES;
         if (want_dk) {
+          // dP^T = V dO^T; dO is then free
+          if (!(ok = mbar_wait_warp(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL)))
+            break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t voff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
@@ -263,33 +372,49 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                    sdesc_sw128(ga + goff, 16, 1024), id_s, kk > 0);
           }
           tc_commit(bar(K_DPF));
-        }
-        // dV += P^T dO   (contraction over the BM queries of this tile)
-        if (want_dv) {
-          if (!(ok = mbar_wait_warp(bar(K_PR), u & 1, abort_flag, ctl, SITE_BWD_P_READY))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk) {
-            // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
-            const int h = (16 * kk) / (C::BM / 2);
-            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + acol,
-                   sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          if (!spill) tc_commit(bar(K_OE + os));   // spill: released after the dS^T store
+          if (more) {
+            if (!(ok = mbar_wait_warp(bar(K_SC), u & 1, abort_flag, ctl, SITE_BWD_S_READ))) break;
+            if (!(ok = mbar_wait_warp(bar(K_QF + qn), pn, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
+            tc_fence_after();
+            issue_s(u + 1, C::S_COL);
+            tc_commit(bar(K_SF));
           }
-        }
-        // dK += dS^T Q
-        if (want_dk) {
+          // dK += dS^T Q; Q is then free
           if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < C::BM / 16; ++kk) {
             const int h = (16 * kk) / (C::BM / 2);
             const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + acol,
+            mma_ts(tmem + C::ACC_COL, tmem + C::DP_COL + acol,
                    sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
           }
+          tc_commit(bar(K_QE + qs));
+        } else {
+          if (more) {
+            if (!(ok = mbar_wait_warp(bar(K_QF + qn), pn, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
+            tc_fence_after();
+            issue_s(u + 1, s_col(u + 1));
+            tc_commit(sf_bar(u + 1));
+            tc_commit(bar(K_QE + qn));
+          }
+          // dV += P^T dO  (contraction over the BM queries of this tile); dO is then free
+          if (!(ok = mbar_wait_warp(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL)))
+            break;
+          if (!(ok = mbar_wait_warp(pr_bar(u), (u >> 1) & 1, abort_flag, ctl, SITE_BWD_P_READY)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk) {
+            // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
+            const int h = (16 * kk) / (C::BM / 2);
+            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
+            mma_ts(tmem + C::ACC_COL, tmem + s_col(u) + acol,
+                   sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          }
+          tc_commit(bar(K_OE + os));
         }
-        tc_commit(bar(K_QE + s));
       }
       tc_commit(bar(K_ACC));
       if (__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -306,13 +431,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int key = k0 + r;
     constexpr int NC = C::BM / 2;         // query columns of this thread
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + C::S_COL + h * NC;
     const uint32_t dp_addr = tmem + lane_off + C::DP_COL + h * NC;
     bool ok = true;
-    if (C::K_IN_TMEM && h == 0) {   // first warpgroup: K rows into tensor memory
+    if (h == 0) {   // first warpgroup: K rows into tensor memory
       ok = mbar_wait(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       if (__all_sync(0xffffffffu, ok)) {
-        tile_to_tmem<D>(smem + C::K_LOAD_OFF, tmem + lane_off + C::K_COL, r);
+        tile_to_tmem<D>(smem + k_load, tmem + lane_off + C::K_COL, r);
         tc_fence_before();
         mbar_arrive(bar(K_CP));
       } else {
@@ -321,13 +445,20 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     for (int gi = 0, u = 0; ok && gi < gper; ++gi) {
       for (int ut = 0; ut < cnt; ++ut, ++u) {
-        const int s = u % C::STG;
+        const int qs = u % C::QSL, os = u % C::OSL;
         const int q0 = qtile(ut) * C::BM;
-        const uint8_t* stp = smem + C::ST_OFF + s * C::STAGE;
-        const float* lse2 = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES) + h * NC;
-        const float* dd = reinterpret_cast<const float*>(stp + 2 * C::QT_BYTES + 512) + h * NC;
-        ok = mbar_wait(bar(K_QF + s), (u / C::STG) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
-        ok = ok && mbar_wait(bar(K_SF), u & 1, abort_flag, ctl, SITE_BWD_S_FULL);
+        const uint32_t s_addr = tmem + lane_off + s_col(u) + h * NC;
+        // LSE2 (and D): with Q in the dK CTA, with dO in the dV CTA
+        const float* lse2;
+        if (want_dk) {
+          lse2 = reinterpret_cast<const float*>(smem + C::QST_OFF + qs * 2 * C::STAT_BYTES) + h * NC;
+          ok = mbar_wait(bar(K_QF + qs), (u / C::QSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+        } else {
+          lse2 = reinterpret_cast<const float*>(smem + C::OST_OFF + os * C::STAT_BYTES) + h * NC;
+          ok = mbar_wait(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL);
+        }
+        const float* dd = lse2 + C::BM;
+        ok = ok && mbar_wait(sf_bar(u), sf_par(u), abort_flag, ctl, SITE_BWD_S_FULL);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const bool masked = causal && (k0 + C::BNK - 1 > q0);
@@ -345,6 +476,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             p[c0 + i] = v;
           }
         }
+        if (want_dk) {   // S^T has been read: its columns take the next tile's S^T
+          tc_fence_before();
+          mbar_arrive(bar(K_SC));
+        }
         if constexpr (KR < C::BNK) {   // keys of the next study tile: no contribution
           if (r >= KR) {
 #pragma unroll
@@ -361,9 +496,9 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(bar(K_PR));
+          mbar_arrive(pr_bar(u));
+          continue;   // the dV CTA forms no dP, no dS
         }
-        if (!want_dk) continue;   // SPLIT_OUT, dV CTA: no dP, no dS
         ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -387,40 +522,36 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           for (int i = 0; i < 16; ++i) pk[i] = ds[c0 + i];
           tmem_st16(dp_addr + c0, pk);
         }
-        if (!GROUPED && !SPARSE && dSt != nullptr && key < n && (KR == C::BNK || r < KR)) {
-          // dS^T row of this key, queries [qbase, qbase + NC): dQ = scale dS K
-          // is then one GEMM (the dQ mode "spill"); rows are 16-byte aligned
-          __nv_bfloat16* row = dSt + ((size_t)bh * n + key) * ld_ds + qbase;
-          if (qbase + NC <= n) {
-#pragma unroll
-            for (int c = 0; c < NC / 8; ++c)
-              reinterpret_cast<uint4*>(row)[c] =
-                  make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
-          } else {
-            for (int c = 0; qbase + c < n; ++c)
-              row[c] = __ushort_as_bfloat16((unsigned short)(ds[c >> 1] >> (16 * (c & 1))));
-          }
-        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(K_DSR));
+        if (spill) {
+          // dS^T rows of queries [h NC, h NC + NC) into the consumed dO slot
+          // as one 128-byte-swizzled [128 keys][64 queries] box
+          uint8_t* stg = smem + C::OS_OFF + os * C::QT_BYTES;
+#pragma unroll
+          for (int j = 0; j < NC / 8; ++j)
+            *reinterpret_cast<uint4*>(stg + sw128_offset(r, h * (NC / 8) + j)) =
+                make_uint4(ds[4 * j], ds[4 * j + 1], ds[4 * j + 2], ds[4 * j + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(bar(K_DSS + os));
+        }
       }
     }
-    // ---- epilogue: SPLIT_OUT: warpgroup h writes columns [h d/2, (h+1) d/2)
-    // of this CTA's output; otherwise half 0 writes dV and half 1 dK (scaled)
+    // ---- epilogue: warpgroup h writes columns [h d/2, (h+1) d/2) of this
+    // CTA's output (dK scaled)
     if (ok) {
       ok = mbar_wait(bar(K_ACC), 0, abort_flag, ctl, SITE_BWD_ACC_DONE);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      const bool out_dv = C::SPLIT_OUT ? want_dv : h == 0;
-      constexpr int W = C::SPLIT_OUT ? D / 2 : C::DO;   // columns of this warpgroup
-      const int c_first = C::SPLIT_OUT ? h * W : 0;
-      const uint32_t src = tmem + lane_off + (out_dv ? C::DV_COL : C::DK_COL) + c_first;
+      constexpr int W = D / 2;   // columns of this warpgroup
+      const int c_first = h * W;
+      const uint32_t src = tmem + lane_off + C::ACC_COL + c_first;
       const size_t off = ((size_t)bh * n + key) * D + c_first;
-      const float mul = out_dv ? 1.f : scale;
-      float* acc = GROUPED ? (out_dv ? dVacc : dKacc) : nullptr;   // set when the group is split
+      const float mul = want_dv ? 1.f : scale;
+      float* acc = GROUPED ? (want_dv ? dVacc : dKacc) : nullptr;   // set when the group is split
 #pragma unroll 1
       for (int c0 = 0; c0 < W; c0 += 32) {
         uint32_t rr[32];
@@ -438,7 +569,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                          mul * __uint_as_float(rr[i + 1]), mul * __uint_as_float(rr[i + 2]),
                          mul * __uint_as_float(rr[i + 3]));
           } else {
-            store32_bf16((out_dv ? dV : dK) + off + c0, rr, mul);
+            store32_bf16((want_dv ? dV : dK) + off + c0, rr, mul);
           }
         }
       }
@@ -727,7 +858,13 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
       !make_tmap_bf16(&tv, V, D, n, BHkv, 64, C::BNK) ||
       !make_tmap_bf16(&tg, dO, D, n, BH, 64, C::BM))
     return ATTN_ERR_CUDA;
+  // dS^T for the dQ mode "spill": [BH][n keys][n queries], rows ld_ds apart;
+  // stores are clipped at n in both dimensions
+  CUtensorMap ts;
+  std::memset(&ts, 0, sizeof(ts));
+  if (dSt && !make_tmap_bf16(&ts, dSt, n, n, BH, 64, C::BNK, ld_ds)) return ATTN_ERR_CUDA;
   if (tl.lists && hm.group > 1) return ATTN_ERR_UNSUPPORTED;
+  if (dSt && (tl.lists || hm.group > 1 || KR != C::BNK)) return ATTN_ERR_UNSUPPORTED;
   auto kern = bwd_kv_kernel<D, false, false, KR>;
   if constexpr (KR == C::BNK) {
     if (tl.lists) kern = bwd_kv_kernel<D, false, true>;
@@ -744,8 +881,8 @@ int launch_kv_cfg(const void* Q, const void* K, const void* V, const void* dO, c
                                            static_cast<__nv_bfloat16*>(dK),
                                            static_cast<__nv_bfloat16*>(dV), dKacc, dVacc, hm,
                                            gsplit, tl, n, n_pad, scale,
-                                           scale * 1.4426950408889634f, causal, ctl,
-                                           static_cast<__nv_bfloat16*>(dSt), ld_ds);
+                                           scale * 1.4426950408889634f, causal, ctl, ts,
+                                           dSt != nullptr ? 1 : 0);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

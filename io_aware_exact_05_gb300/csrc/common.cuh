@@ -55,6 +55,7 @@ enum WaitSite : int {
   SITE_BWD_ACC_DONE = 210,
   SITE_BWD_DS_FREE = 211,
   SITE_BWD_SMEM_ALIGN = 212,   // shared-memory base not 1024-byte aligned (not a wait)
+  SITE_BWD_S_READ = 213,       // the compute warps have taken S into registers
   SITE_GEMM_FULL = 301,
   SITE_GEMM_EMPTY = 302,
   SITE_GEMM_ACC = 303,
