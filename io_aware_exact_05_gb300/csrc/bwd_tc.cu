@@ -328,16 +328,35 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       constexpr uint32_t id_acc = idesc_bf16(128, C::DO, false, true);  // P^T/dS^T TMEM, dO/Q MN-major
       bool ok = mbar_wait_warp(bar(K_KV), 0, abort_flag, ctl, SITE_BWD_KV);
       ok = ok && mbar_wait_warp(bar(K_CP), 0, abort_flag, ctl, SITE_BWD_KV);
-      const uint32_t va = sb + C::V_OFF;
+      // MMAs in groups of four from one asm block, with the shared-memory
+      // descriptors' low halves precomputed (the MMA queue is shallow, so
+      // scalar work between MMAs costs tensor time)
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t QT16 = C::QT_BYTES >> 4;
+      const uint32_t v_km = sdesc_lo(sb + C::V_OFF, 16);                // V, K-major
+      const uint32_t q_km = sdesc_lo(sb + C::QS_OFF, 16);               // Q slot 0, K-major
+      const uint32_t q_mn = sdesc_lo(sb + C::QS_OFF, C::BM * 128);      // Q slot 0, MN-major
+      const uint32_t g_km = sdesc_lo(sb + C::OS_OFF, 16);               // dO slot 0, K-major
+      const uint32_t g_mn = sdesc_lo(sb + C::OS_OFF, C::BM * 128);      // dO slot 0, MN-major
+      // K-major operand, 64-wide column box b of a tile with `rows` rows
+      auto km4 = [](uint32_t base, int rows, int b, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + b * (rows * 128 / 16) + 2 * i;
+      };
+      // MN-major operand, K slices 0..3 (16 rows = 2048 bytes each)
+      auto mn4 = [](uint32_t base, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + i * (2048 / 16);
+      };
       // S^T(u) = K Q_u^T into column col: A = K from tensor memory (16
       // elements = 8 columns per MMA), contraction over d
       auto issue_s = [&](int u, int col) {
-        const uint32_t qa = sb + C::QS_OFF + (u % C::QSL) * C::QT_BYTES;
+        const uint32_t qb = q_km + (u % C::QSL) * QT16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          mma_ts(tmem + col, tmem + C::K_COL + 8 * kk, sdesc_sw128(qa + qoff, 16, 1024), id_s,
-                 kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {
+          uint32_t blo[4];
+          km4(qb, C::BM, b, blo);
+          mma_ts_x4(tmem + col, tmem + C::K_COL + 32 * b, blo, HI, id_s, b > 0);
         }
       };
       // S^T of the next tile is issued before this tile's accumulator
@@ -357,19 +376,17 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int qs = u % C::QSL, os = u % C::OSL;
         const int qn = (u + 1) % C::QSL, pn = ((u + 1) / C::QSL) & 1;
         const bool more = u + 1 < total;
-        const uint32_t qa = sb + C::QS_OFF + qs * C::QT_BYTES;
-        const uint32_t ga = sb + C::OS_OFF + os * C::QT_BYTES;
         if (want_dk) {
           // dP^T = V dO^T; dO is then free
           if (!(ok = mbar_wait_warp(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL)))
             break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t voff = (kk >> 2) * (C::BNK * 128) + (kk & 3) * 32;
-            const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::DP_COL, sdesc_sw128(va + voff, 16, 1024),
-                   sdesc_sw128(ga + goff, 16, 1024), id_s, kk > 0);
+          for (int b = 0; b < C::NKB; ++b) {
+            uint32_t alo[4], blo[4];
+            km4(v_km, C::BNK, b, alo);
+            km4(g_km + os * QT16, C::BM, b, blo);
+            mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_s, b > 0);
           }
           tc_commit(bar(K_DPF));
           if (!spill) tc_commit(bar(K_OE + os));   // spill: released after the dS^T store
@@ -383,12 +400,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           // dK += dS^T Q; Q is then free
           if (!(ok = mbar_wait_warp(bar(K_DSR), u & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk) {
-            const int h = (16 * kk) / (C::BM / 2);
-            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-            mma_ts(tmem + C::ACC_COL, tmem + C::DP_COL + acol,
-                   sdesc_sw128(qa + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          {   // dS^T half h (queries [32h, 32h+32)) at columns [32h, 32h+16)
+            uint32_t blo[4];
+            mn4(q_mn + qs * QT16, blo);
+            mma_ts_x4_halves<C::BM / 2>(tmem + C::ACC_COL, tmem + C::DP_COL, blo, HI, id_acc, u > 0);
           }
           tc_commit(bar(K_QE + qs));
         } else {
@@ -405,13 +420,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (!(ok = mbar_wait_warp(pr_bar(u), (u >> 1) & 1, abort_flag, ctl, SITE_BWD_P_READY)))
             break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk) {
-            // queries [16kk, 16kk+16): half h = 16kk / (BM/2) stores them at its own columns
-            const int h = (16 * kk) / (C::BM / 2);
-            const uint32_t acol = h * (C::BM / 2) + ((16 * kk - h * (C::BM / 2)) >> 1);
-            mma_ts(tmem + C::ACC_COL, tmem + s_col(u) + acol,
-                   sdesc_sw128(ga + kk * 2048, C::BM * 128, 1024), id_acc, (u > 0 || kk > 0));
+          {   // P^T half h (queries [32h, 32h+32)) at columns [32h, 32h+16) of the slot
+            uint32_t blo[4];
+            mn4(g_mn + os * QT16, blo);
+            mma_ts_x4_halves<C::BM / 2>(tmem + C::ACC_COL, tmem + s_col(u), blo, HI, id_acc, u > 0);
           }
           tc_commit(bar(K_OE + os));
         }

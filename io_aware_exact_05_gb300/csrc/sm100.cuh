@@ -313,6 +313,29 @@ ATTN_MMA_TS_X4(mma_ts_x4, "1", "f16")
 ATTN_MMA_TS_X4(mma_ts_x4_f8, "1", "f8f6f4")
 #undef ATTN_MMA_TS_X4
 
+// Four bf16 MMAs with A from tensor memory at columns a, a + 8, a + H and
+// a + H + 8: a 64-wide K range held as two 16-column halves H columns apart
+// (P^T or dS^T of a 64-query tile, each half written by its own warpgroup).
+template <int H>
+__device__ __forceinline__ void mma_ts_x4_halves(uint32_t d, uint32_t a_tmem,
+                                                 const uint32_t (&blo)[4], uint32_t bhi,
+                                                 uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 b0, b1, b2, b3;\n\t.reg .b32 x1, x2, x3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 t, %7, %7;\n\t"
+      "mov.b64 b0, {%2, %6};\n\tmov.b64 b1, {%3, %6};\n\t"
+      "mov.b64 b2, {%4, %6};\n\tmov.b64 b3, {%5, %6};\n\t"
+      "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, %9;\n\tadd.u32 x3, %1, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %8, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], b1, %8, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], b2, %8, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], b3, %8, t;\n\t}\n" ::"r"(d),
+      "r"(a_tmem), "r"(blo[0]), "r"(blo[1]), "r"(blo[2]), "r"(blo[3]), "r"(bhi), "r"(acc),
+      "r"(idesc), "n"(H), "n"(H + 8)
+      : "memory");
+}
+
 // Low and high 32-bit halves of the 128-byte-swizzle shared-memory descriptor
 // (same fields as sdesc_sw128).
 __host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
