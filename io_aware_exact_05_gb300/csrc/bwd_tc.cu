@@ -618,6 +618,7 @@ struct QCfg {
   static constexpr int Q_COL = 2 * BN + D;            // Q as A operand (Q_IN_TMEM)
   static constexpr int NTHREADS = 384;
   static_assert(2 * BN + D + (Q_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
+  static_assert(BN == 64 || BN == 128, "dS halves as the dQ product reads them");
   static_assert(!Q_IN_TMEM || QT_BYTES <= 2 * KV_BYTES, "Q fits in the second stage");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -725,40 +726,64 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait_warp(bar(Q_QF), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
       if (C::Q_IN_TMEM) ok = ok && mbar_wait_warp(bar(Q_CP), 0, abort_flag, ctl, SITE_BWD_Q_FULL);
-      const uint32_t qa = sb + C::Q_OFF, ga = sb + C::G_OFF;
+      // MMAs in groups of four from one asm block, with the shared-memory
+      // descriptors' low halves precomputed
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t STG16 = (2 * C::KV_BYTES) >> 4, KV16 = C::KV_BYTES >> 4;
+      const uint32_t q_km = sdesc_lo(sb + C::Q_OFF, 16);              // Q, K-major
+      const uint32_t g_km = sdesc_lo(sb + C::G_OFF, 16);              // dO, K-major
+      const uint32_t st_km = sdesc_lo(sb + C::ST_OFF, 16);            // stage 0 K (V), K-major
+      const uint32_t st_mn = sdesc_lo(sb + C::ST_OFF, C::BN * 128);   // stage 0 K, MN-major
+      auto km4 = [](uint32_t base, int rows, int b, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + b * (rows * 128 / 16) + 2 * i;
+      };
+      auto mn4 = [](uint32_t base, int g, uint32_t (&lo)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = base + (4 * g + i) * (2048 / 16);
+      };
       for (int j = 0; ok && j < cnt; ++j) {
         const int s = j % C::STG;
-        const uint32_t ka = sb + C::ST_OFF + s * 2 * C::KV_BYTES, va = ka + C::KV_BYTES;
         if (!(ok = mbar_wait_warp(bar(Q_KF + s), (j / C::STG) & 1, abort_flag, ctl, SITE_BWD_KV))) break;
         tc_fence_after();
+        const uint32_t kso = s * STG16;
+        // S = Q K_j^T and dP = dO V_j^T  (contraction over d, 64 per group)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-          if (C::Q_IN_TMEM)   // A = Q from tensor memory, 16 elements = 8 columns per MMA
-            mma_ts(tmem + C::S_COL, tmem + C::Q_COL + 8 * kk, sdesc_sw128(ka + koff, 16, 1024),
-                   id_s, kk > 0);
-          else
-            mma_ss(tmem + C::S_COL, sdesc_sw128(qa + qoff, 16, 1024),
-                   sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {
+          uint32_t blo[4];
+          km4(st_km + kso, C::BN, b, blo);
+          if (C::Q_IN_TMEM) {   // A = Q from tensor memory, 16 elements = 8 columns per MMA
+            mma_ts_x4(tmem + C::S_COL, tmem + C::Q_COL + 32 * b, blo, HI, id_s, b > 0);
+          } else {
+            uint32_t alo[4];
+            km4(q_km, C::BM, b, alo);
+            mma_ss_x4(tmem + C::S_COL, alo, HI, blo, HI, id_s, b > 0);
+          }
         }
         tc_commit(bar(Q_SF));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t goff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          const uint32_t voff = (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::DP_COL, sdesc_sw128(ga + goff, 16, 1024), sdesc_sw128(va + voff, 16, 1024),
-                 id_s, kk > 0);
+        for (int b = 0; b < C::NKB; ++b) {
+          uint32_t alo[4], blo[4];
+          km4(g_km, C::BM, b, alo);
+          km4(st_km + kso + KV16, C::BN, b, blo);
+          mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_s, b > 0);
         }
         tc_commit(bar(Q_DPF));
         if (!(ok = mbar_wait_warp(bar(Q_DSR), j & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
+        // dQ += dS K_j: dS half h (keys [h BN/2, (h+1) BN/2)) at columns
+        // [h BN/2, h BN/2 + BN/4) of the S slot
+        if constexpr (C::BN == 64) {
+          uint32_t blo[4];
+          mn4(st_mn + kso, 0, blo);
+          mma_ts_x4_halves<C::BN / 2>(tmem + C::DQ_COL, tmem + C::S_COL, blo, HI, id_dq, j > 0);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const int h = (16 * kk) / (C::BN / 2);
-          const uint32_t acol = h * (C::BN / 2) + ((16 * kk - h * (C::BN / 2)) >> 1);
-          mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + acol,
-                 sdesc_sw128(ka + kk * 2048, C::BN * 128, 1024), id_dq, (j > 0 || kk > 0));
+          for (int g = 0; g < C::BN / 64; ++g) {
+            uint32_t blo[4];
+            mn4(st_mn + kso, g, blo);
+            mma_ts_x4(tmem + C::DQ_COL, tmem + C::S_COL + 64 * g, blo, HI, id_dq, (j > 0 || g > 0));
+          }
         }
         tc_commit(bar(Q_KE + s));
       }

@@ -27,6 +27,7 @@ using namespace sm100;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
+static_assert(kBK == 64, "four K slices of 16 per staged block");
 
 template <int BN, int STG = kStages>
 struct GemmLayout {
@@ -49,10 +50,10 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
 //  K-major: rows of 64 K elements (128 B); the slice starts 32 B further.
 //  MN-major: rows of 64 M/N elements, one per k; the slice starts 16 rows
 //  (2048 B) further; 64-wide M/N blocks are `mn_block_bytes` apart.
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int kk,
-                                                 uint32_t mn_block_bytes) {
-  return kmajor ? sdesc_sw128(base + kk * 32, 16, 1024)
-                : sdesc_sw128(base + kk * 2048, mn_block_bytes, 1024);
+// (Low half; the high half is sdesc_hi(1024) in both cases.)
+__device__ __forceinline__ uint32_t operand_lo(uint32_t base, bool kmajor, int kk,
+                                               uint32_t mn_block_bytes) {
+  return kmajor ? sdesc_lo(base + kk * 32, 16) : sdesc_lo(base + kk * 2048, mn_block_bytes);
 }
 
 template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages, bool TMA_C = true>
@@ -135,11 +136,14 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
       if (!mbar_wait_warp(full(s), (kb / kStages) & 1, abort_flag, ctl, SITE_GEMM_FULL)) break;
       tc_fence_after();
       const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
+      // the block's four K slices from one asm block
+      uint32_t alo[4], blo[4];
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        mma_ss(tmem, operand_desc(sa, A_K, kk, 8192), operand_desc(sb, B_K, kk, 8192), idesc,
-               (kb | kk) != 0);
+        alo[kk] = operand_lo(sa, A_K, kk, 8192);
+        blo[kk] = operand_lo(sb, B_K, kk, 8192);
       }
+      mma_ss_x4(tmem, alo, sdesc_hi(1024), blo, sdesc_hi(1024), idesc, kb != 0);
       tc_commit(empty(s));
     }
     tc_commit(acc_bar);
