@@ -46,10 +46,6 @@ namespace {
 
 using namespace sm100;
 
-__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
   uint32_t pk[16];
 #pragma unroll
@@ -598,33 +594,41 @@ template <int D>
 struct QCfg {
   static constexpr int BM = 128;                     // queries per CTA (TMEM lanes)
   static constexpr int BN = (D == 256) ? 64 : 128;   // keys per iteration
-  static constexpr int STG = 2;
+  // K_j and V_j in separate rings, each slot released by its last reader
+  // (K_j after dQ(j), V_j after dP(j)); three K slots give the load of
+  // K_{j+1} a whole iteration, since S(j+1) is issued before dQ(j)
+  static constexpr int KSL = 3;
+  static constexpr int VSL = 2;
   // d = 256: Q (the A operand of S = Q K^T, constant for the CTA) lives in
-  // tensor memory, which frees the shared memory of a second K/V stage
+  // tensor memory, which frees the shared memory of the rings
   static constexpr bool Q_IN_TMEM = (D == 256);
   static constexpr int NKB = D / 64;
   static constexpr uint32_t QT_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
   static constexpr uint32_t Q_OFF = 0;                              // unused when Q_IN_TMEM
   static constexpr uint32_t G_OFF = Q_IN_TMEM ? 0 : QT_BYTES;
-  static constexpr uint32_t ST_OFF = Q_IN_TMEM ? QT_BYTES : 2 * QT_BYTES;   // (K_j, V_j) stages
-  // where Q's load lands: the second stage, before that stage's first use
-  static constexpr uint32_t Q_LOAD_OFF = Q_IN_TMEM ? ST_OFF + 2 * KV_BYTES : Q_OFF;
-  static constexpr uint32_t BAR_OFF = ST_OFF + STG * 2 * KV_BYTES;
-  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t KS_OFF = G_OFF + QT_BYTES;              // K slots
+  static constexpr uint32_t VS_OFF = KS_OFF + KSL * KV_BYTES;       // V slots
+  // where Q's load lands: K slots 1 and 2, before their first use
+  static constexpr uint32_t Q_LOAD_OFF = Q_IN_TMEM ? KS_OFF + KV_BYTES : Q_OFF;
+  static constexpr uint32_t BAR_OFF = VS_OFF + VSL * KV_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + 256;    // base must be 1024-byte aligned
   static constexpr int S_COL = 0;
-  static constexpr int DP_COL = BN;
+  static constexpr int DP_COL = BN;                   // dP, then dS in bf16 over it
   static constexpr int DQ_COL = 2 * BN;
   static constexpr int Q_COL = 2 * BN + D;            // Q as A operand (Q_IN_TMEM)
   static constexpr int NTHREADS = 384;
   static_assert(2 * BN + D + (Q_IN_TMEM ? D / 2 : 0) <= 512, "tensor memory budget");
   static_assert(BN == 64 || BN == 128, "dS halves as the dQ product reads them");
-  static_assert(!Q_IN_TMEM || QT_BYTES <= 2 * KV_BYTES, "Q fits in the second stage");
+  static_assert(!Q_IN_TMEM || QT_BYTES <= 2 * KV_BYTES, "Q's load fits in K slots 1 and 2");
+  static_assert(KV_BYTES % 1024 == 0 && QT_BYTES % 1024 == 0, "slots stay 1024-byte aligned");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum : int { Q_QF = 0, Q_KF = 1, Q_KE = 3, Q_SF = 5, Q_DPF = 6, Q_DSR = 7, Q_ACC = 8, Q_DRAIN = 9,
-             Q_CP = 10 };
+// Q_SC: the compute warps hold P of the current key tile in registers, so the
+// S columns are free for the next tile's S.
+enum : int { Q_QF = 0, Q_KF = 1, Q_KE = 4, Q_VF = 7, Q_VE = 9, Q_SF = 11, Q_DPF = 12, Q_DSR = 13,
+             Q_ACC = 14, Q_DRAIN = 15, Q_CP = 16, Q_SC = 17 };
 
 template <int D>
 __global__ void __launch_bounds__(QCfg<D>::NTHREADS, 1)
@@ -635,7 +639,13 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
              float scale, float scale_log2, int causal, KernelCtl ctl) {
   using C = QCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1k(smem_raw);
+  // no room to align the layout: it needs the base 1024-byte aligned (the
+  // 128-byte swizzle atoms); report and leave before touching anything
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(ctl, ATTN_ERR_CUDA, SITE_BWD_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -664,13 +674,18 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QF), 1);
-    for (int s = 0; s < C::STG; ++s) {
+    for (int s = 0; s < C::KSL; ++s) {
       mbar_init(bar(Q_KF + s), 1);
       mbar_init(bar(Q_KE + s), 1);
+    }
+    for (int s = 0; s < C::VSL; ++s) {
+      mbar_init(bar(Q_VF + s), 1);
+      mbar_init(bar(Q_VE + s), 1);
     }
     mbar_init(bar(Q_SF), 1);
     mbar_init(bar(Q_DPF), 1);
     mbar_init(bar(Q_DSR), 256);
+    mbar_init(bar(Q_SC), 256);
     mbar_init(bar(Q_ACC), 1);
     mbar_init(bar(Q_DRAIN), 1);
     mbar_init(bar(Q_CP), 128);
@@ -689,36 +704,56 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 
   if (warp < 4) {
     if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ Q, dO and K producer
       mbar_expect_tx(bar(Q_QF), 2 * C::QT_BYTES);
 #pragma unroll
       for (int kb = 0; kb < C::NKB; ++kb) {
         tma_load_3d(sb + C::Q_LOAD_OFF + kb * (C::BM * 128), &tmQ, kb * 64, q0, bh, bar(Q_QF));
         tma_load_3d(sb + C::G_OFF + kb * (C::BM * 128), &tmdO, kb * 64, q0, bh, bar(Q_QF));
       }
-      int issued_last[2] = {-1, -1};
+      int k_last[C::KSL];
+      for (int s = 0; s < C::KSL; ++s) k_last[s] = -1;
       for (int j = 0; j < cnt; ++j) {
-        const int s = j % C::STG;
-        if (!mbar_wait(bar(Q_KE + s), ((j / C::STG) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+        const int s = j % C::KSL;
+        if (!mbar_wait(bar(Q_KE + s), ((j / C::KSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
           break;
-        // the second stage holds Q until it has been copied to tensor memory
+        // K slots 1 and 2 hold Q until it has been copied to tensor memory
         if (C::Q_IN_TMEM && j == 1 && !mbar_wait(bar(Q_CP), 0, abort_flag, ctl, SITE_BWD_Q_FULL))
           break;
-        const uint32_t st = sb + C::ST_OFF + s * 2 * C::KV_BYTES;
-        mbar_expect_tx(bar(Q_KF + s), 2 * C::KV_BYTES);
+        const uint32_t kd = sb + C::KS_OFF + s * C::KV_BYTES;
+        mbar_expect_tx(bar(Q_KF + s), C::KV_BYTES);
 #pragma unroll
-        for (int kb = 0; kb < C::NKB; ++kb) {
-          tma_load_3d(st + kb * (C::BN * 128), &tmK, kb * 64, ktile(j) * C::BN, bkv, bar(Q_KF + s));
-          tma_load_3d(st + C::KV_BYTES + kb * (C::BN * 128), &tmV, kb * 64, ktile(j) * C::BN, bkv,
-                      bar(Q_KF + s));
-        }
-        issued_last[s] = j;
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_3d(kd + kb * (C::BN * 128), &tmK, kb * 64, ktile(j) * C::BN, bkv, bar(Q_KF + s));
+        k_last[s] = j;
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         mbar_wait(bar(Q_QF), 0, &no_abort, ctl, SITE_BWD_Q_FULL);
-        for (int s = 0; s < C::STG; ++s)
-          if (issued_last[s] >= 0)
-            mbar_wait(bar(Q_KF + s), (issued_last[s] / C::STG) & 1, &no_abort, ctl, SITE_BWD_KV);
+        for (int s = 0; s < C::KSL; ++s)
+          if (k_last[s] >= 0)
+            mbar_wait(bar(Q_KF + s), (k_last[s] / C::KSL) & 1, &no_abort, ctl, SITE_BWD_KV);
+      }
+    } else if (warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ V producer
+      int v_last[C::VSL];
+      for (int s = 0; s < C::VSL; ++s) v_last[s] = -1;
+      for (int j = 0; j < cnt; ++j) {
+        const int s = j % C::VSL;
+        if (!mbar_wait(bar(Q_VE + s), ((j / C::VSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY))
+          break;
+        const uint32_t vd = sb + C::VS_OFF + s * C::KV_BYTES;
+        mbar_expect_tx(bar(Q_VF + s), C::KV_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_3d(vd + kb * (C::BN * 128), &tmV, kb * 64, ktile(j) * C::BN, bkv, bar(Q_VF + s));
+        v_last[s] = j;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < C::VSL; ++s)
+          if (v_last[s] >= 0)
+            mbar_wait(bar(Q_VF + s), (v_last[s] / C::VSL) & 1, &no_abort, ctl, SITE_BWD_KV);
       }
     } else if (warp == 1) {
       // MMA issuer (the whole warp runs the loop; one elected lane issues)
@@ -729,11 +764,12 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       // MMAs in groups of four from one asm block, with the shared-memory
       // descriptors' low halves precomputed
       constexpr uint32_t HI = sdesc_hi(1024);
-      constexpr uint32_t STG16 = (2 * C::KV_BYTES) >> 4, KV16 = C::KV_BYTES >> 4;
+      constexpr uint32_t KV16 = C::KV_BYTES >> 4;
       const uint32_t q_km = sdesc_lo(sb + C::Q_OFF, 16);              // Q, K-major
       const uint32_t g_km = sdesc_lo(sb + C::G_OFF, 16);              // dO, K-major
-      const uint32_t st_km = sdesc_lo(sb + C::ST_OFF, 16);            // stage 0 K (V), K-major
-      const uint32_t st_mn = sdesc_lo(sb + C::ST_OFF, C::BN * 128);   // stage 0 K, MN-major
+      const uint32_t k_km = sdesc_lo(sb + C::KS_OFF, 16);             // K slot 0, K-major
+      const uint32_t k_mn = sdesc_lo(sb + C::KS_OFF, C::BN * 128);    // K slot 0, MN-major
+      const uint32_t v_km = sdesc_lo(sb + C::VS_OFF, 16);             // V slot 0, K-major
       auto km4 = [](uint32_t base, int rows, int b, uint32_t (&lo)[4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) lo[i] = base + b * (rows * 128 / 16) + 2 * i;
@@ -742,16 +778,13 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 #pragma unroll
         for (int i = 0; i < 4; ++i) lo[i] = base + (4 * g + i) * (2048 / 16);
       };
-      for (int j = 0; ok && j < cnt; ++j) {
-        const int s = j % C::STG;
-        if (!(ok = mbar_wait_warp(bar(Q_KF + s), (j / C::STG) & 1, abort_flag, ctl, SITE_BWD_KV))) break;
-        tc_fence_after();
-        const uint32_t kso = s * STG16;
-        // S = Q K_j^T and dP = dO V_j^T  (contraction over d, 64 per group)
+      // S = Q K_j^T into the S columns  (contraction over d, 64 per group)
+      auto issue_s = [&](int j) {
+        const uint32_t kb0 = k_km + (j % C::KSL) * KV16;
 #pragma unroll
         for (int b = 0; b < C::NKB; ++b) {
           uint32_t blo[4];
-          km4(st_km + kso, C::BN, b, blo);
+          km4(kb0, C::BN, b, blo);
           if (C::Q_IN_TMEM) {   // A = Q from tensor memory, 16 elements = 8 columns per MMA
             mma_ts_x4(tmem + C::S_COL, tmem + C::Q_COL + 32 * b, blo, HI, id_s, b > 0);
           } else {
@@ -760,32 +793,59 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             mma_ss_x4(tmem + C::S_COL, alo, HI, blo, HI, id_s, b > 0);
           }
         }
-        tc_commit(bar(Q_SF));
+      };
+      // dS goes over dP, so S of the next key tile is issued as soon as the
+      // compute warps hold P in registers (Q_SC): the pipe runs dP(j),
+      // S(j+1), dQ(j) back to back while they form dS(j).
+      if (ok && cnt > 0) {
+        ok = mbar_wait_warp(bar(Q_KF), 0, abort_flag, ctl, SITE_BWD_KV);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          tc_commit(bar(Q_SF));
+        }
+      }
+      for (int j = 0; ok && j < cnt; ++j) {
+        const int ks = j % C::KSL, vs = j % C::VSL;
+        // dP = dO V_j^T; V_j is then free
+        if (!(ok = mbar_wait_warp(bar(Q_VF + vs), (j / C::VSL) & 1, abort_flag, ctl, SITE_BWD_KV)))
+          break;
+        tc_fence_after();
 #pragma unroll
         for (int b = 0; b < C::NKB; ++b) {
           uint32_t alo[4], blo[4];
           km4(g_km, C::BM, b, alo);
-          km4(st_km + kso + KV16, C::BN, b, blo);
+          km4(v_km + vs * KV16, C::BN, b, blo);
           mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_s, b > 0);
         }
         tc_commit(bar(Q_DPF));
+        tc_commit(bar(Q_VE + vs));
+        if (j + 1 < cnt) {
+          if (!(ok = mbar_wait_warp(bar(Q_SC), j & 1, abort_flag, ctl, SITE_BWD_S_READ))) break;
+          if (!(ok = mbar_wait_warp(bar(Q_KF + (j + 1) % C::KSL), ((j + 1) / C::KSL) & 1, abort_flag,
+                                    ctl, SITE_BWD_KV)))
+            break;
+          tc_fence_after();
+          issue_s(j + 1);
+          tc_commit(bar(Q_SF));
+        }
+        // dQ += dS K_j: dS half h (keys [h BN/2, (h+1) BN/2)) at columns
+        // [h BN/2, h BN/2 + BN/4) over dP; K_j is then free
         if (!(ok = mbar_wait_warp(bar(Q_DSR), j & 1, abort_flag, ctl, SITE_BWD_DS_READY))) break;
         tc_fence_after();
-        // dQ += dS K_j: dS half h (keys [h BN/2, (h+1) BN/2)) at columns
-        // [h BN/2, h BN/2 + BN/4) of the S slot
         if constexpr (C::BN == 64) {
           uint32_t blo[4];
-          mn4(st_mn + kso, 0, blo);
-          mma_ts_x4_halves<C::BN / 2>(tmem + C::DQ_COL, tmem + C::S_COL, blo, HI, id_dq, j > 0);
+          mn4(k_mn + ks * KV16, 0, blo);
+          mma_ts_x4_halves<C::BN / 2>(tmem + C::DQ_COL, tmem + C::DP_COL, blo, HI, id_dq, j > 0);
         } else {
 #pragma unroll
           for (int g = 0; g < C::BN / 64; ++g) {
             uint32_t blo[4];
-            mn4(st_mn + kso, g, blo);
-            mma_ts_x4(tmem + C::DQ_COL, tmem + C::S_COL + 64 * g, blo, HI, id_dq, (j > 0 || g > 0));
+            mn4(k_mn + ks * KV16, g, blo);
+            mma_ts_x4(tmem + C::DQ_COL, tmem + C::DP_COL + 64 * g, blo, HI, id_dq, (j > 0 || g > 0));
           }
         }
-        tc_commit(bar(Q_KE + s));
+        tc_commit(bar(Q_KE + ks));
       }
       tc_commit(bar(Q_ACC));
       if (__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -816,7 +876,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         ok = false;
       }
     }
-    for (int j = 0; j < cnt; ++j) {
+    for (int j = 0; ok && j < cnt; ++j) {
       const int k0 = ktile(j) * C::BN;
       ok = mbar_wait(bar(Q_SF), j & 1, abort_flag, ctl, SITE_BWD_S_FULL);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -836,6 +896,8 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
           p[c0 + i] = v;
         }
       }
+      tc_fence_before();   // S has been read: its columns take the next key tile's S
+      mbar_arrive(bar(Q_SC));
       ok = mbar_wait(bar(Q_DPF), j & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -848,7 +910,7 @@ bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(p[c0 + 2 * i] * (__uint_as_float(rr[2 * i]) - dd),
                               p[c0 + 2 * i + 1] * (__uint_as_float(rr[2 * i + 1]) - dd));
-        tmem_st16(s_addr + c0 / 2, pk);   // dS over this half's own S columns
+        tmem_st16(dp_addr + c0 / 2, pk);   // dS over this half's own dP columns
       }
       tmem_st_wait();
       tc_fence_before();
