@@ -104,9 +104,11 @@ struct KvCfg {
 
 // K_DSS (dQ mode "spill", one per dO slot): the compute warps have staged
 // dS^T of the tile in that slot for the TMA store.
+// K_DPF: one per dO slot (in the dK CTA's pass mode the dO slot is free once
+// dP^T is).  K_PR: one per Q slot (in the dV CTA the Q slot is free once the
+// compute warps have read S^T).
 enum : int { K_KV = 0, K_QF = 1, K_QE = 4, K_OF = 7, K_OE = 9, K_SF = 11, K_SF1 = 12, K_DPF = 13,
-             K_PR = 14, K_PR1 = 15, K_SC = 16, K_DSR = 17, K_ACC = 18, K_DRAIN = 19, K_CP = 20,
-             K_DSS = 21 };
+             K_PR = 15, K_SC = 18, K_DSR = 19, K_ACC = 20, K_DRAIN = 21, K_CP = 22, K_DSS = 23 };
 
 // GROUPED: query heads share key/value heads (compiled separately so that the
 // one-head-per-head kernel keeps its simple loops).  SPARSE: the CTA walks
@@ -140,8 +142,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 200);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 248);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
   // Causal or block-sparse (tiles of unequal length): heads vary fastest in
@@ -185,7 +187,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   auto s_col = [&](int u) { return (want_dk || !(u & 1)) ? C::S_COL : C::DP_COL; };
   auto sf_bar = [&](int u) { return (want_dk || !(u & 1)) ? bar(K_SF) : bar(K_SF1); };
   auto sf_par = [&](int u) { return want_dk ? (u & 1) : ((u >> 1) & 1); };
-  auto pr_bar = [&](int u) { return (u & 1) ? bar(K_PR1) : bar(K_PR); };
+  auto pr_bar = [&](int u) { return bar(K_PR + u % C::QSL); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(K_KV), 1);
@@ -200,9 +202,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     mbar_init(bar(K_SF), 1);
     mbar_init(bar(K_SF1), 1);
-    mbar_init(bar(K_DPF), 1);
-    mbar_init(bar(K_PR), 256);
-    mbar_init(bar(K_PR1), 256);
+    for (int s = 0; s < C::OSL; ++s) mbar_init(bar(K_DPF + s), 1);
+    for (int s = 0; s < C::QSL; ++s) mbar_init(bar(K_PR + s), 256);
     mbar_init(bar(K_SC), 256);
     mbar_init(bar(K_DSR), 256);
     mbar_init(bar(K_ACC), 1);
@@ -241,7 +242,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int ut = 0; ut < cnt; ++ut, ++u) {
           const int qs = u % C::QSL;
           const int q0 = qtile(ut) * C::BM;
-          if (!mbar_wait(bar(K_QE + qs), ((u / C::QSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+          // the slot's previous tile is done: after dK in the dK CTA, after
+          // the compute warps read S^T ("P ready") in the dV CTA
+          if (!mbar_wait(want_dk ? bar(K_QE + qs) : pr_bar(u), ((u / C::QSL) & 1) ^ 1, abort_flag, ctl,
+                         SITE_BWD_Q_EMPTY)) {
             go = false;
             break;
           }
@@ -282,7 +286,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int ut = 0; ut < cnt; ++ut, ++u) {
           const int os = u % C::OSL;
           const int q0 = qtile(ut) * C::BM;
-          if (!mbar_wait(bar(K_OE + os), ((u / C::OSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
+          // the slot's previous tile is done: after dP^T in the dK CTA (after
+          // its dS^T store in the spill mode), after dV in the dV CTA
+          const uint32_t free_bar = (want_dk && !spill) ? bar(K_DPF + os) : bar(K_OE + os);
+          if (!mbar_wait(free_bar, ((u / C::OSL) & 1) ^ 1, abort_flag, ctl, SITE_BWD_Q_EMPTY)) {
             go = false;
             break;
           }
@@ -365,7 +372,6 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tc_fence_after();
           issue_s(0, s_col(0));
           tc_commit(sf_bar(0));
-          if (want_dv) tc_commit(bar(K_QE));   // the dV CTA reads Q only in S^T
         }
       }
       for (int u = 0; ok && u < total; ++u) {
@@ -384,8 +390,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             km4(g_km + os * QT16, C::BM, b, blo);
             mma_ss_x4(tmem + C::DP_COL, alo, HI, blo, HI, id_s, b > 0);
           }
-          tc_commit(bar(K_DPF));
-          if (!spill) tc_commit(bar(K_OE + os));   // spill: released after the dS^T store
+          tc_commit(bar(K_DPF + os));   // also frees the dO slot (spill: after the dS^T store)
           if (more) {
             if (!(ok = mbar_wait_warp(bar(K_SC), u & 1, abort_flag, ctl, SITE_BWD_S_READ))) break;
             if (!(ok = mbar_wait_warp(bar(K_QF + qn), pn, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
@@ -403,17 +408,18 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
           tc_commit(bar(K_QE + qs));
         } else {
+          // dO(u) (loaded long before) is waited for ahead of S^T(u+1), so
+          // that only "P ready" stands between S^T(u+1) and dV(u)
+          if (!(ok = mbar_wait_warp(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL)))
+            break;
           if (more) {
             if (!(ok = mbar_wait_warp(bar(K_QF + qn), pn, abort_flag, ctl, SITE_BWD_Q_FULL))) break;
             tc_fence_after();
             issue_s(u + 1, s_col(u + 1));
             tc_commit(sf_bar(u + 1));
-            tc_commit(bar(K_QE + qn));
           }
           // dV += P^T dO  (contraction over the BM queries of this tile); dO is then free
-          if (!(ok = mbar_wait_warp(bar(K_OF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_Q_FULL)))
-            break;
-          if (!(ok = mbar_wait_warp(pr_bar(u), (u >> 1) & 1, abort_flag, ctl, SITE_BWD_P_READY)))
+          if (!(ok = mbar_wait_warp(pr_bar(u), (u / C::QSL) & 1, abort_flag, ctl, SITE_BWD_P_READY)))
             break;
           tc_fence_after();
           {   // P^T half h (queries [32h, 32h+32)) at columns [32h, 32h+16) of the slot
@@ -507,7 +513,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           mbar_arrive(pr_bar(u));
           continue;   // the dV CTA forms no dP, no dS
         }
-        ok = mbar_wait(bar(K_DPF), u & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
+        ok = mbar_wait(bar(K_DPF + os), (u / C::OSL) & 1, abort_flag, ctl, SITE_BWD_DP_FULL);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t ds[NC / 2];
