@@ -29,9 +29,13 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 static_assert(kBK == 64, "four K slices of 16 per staged block");
 
-template <int BN, int STG = kStages>
+// MT: 128-row M tiles per CTA, each with its own BN-column accumulator, all
+// fed by the same staged B block (MT = 2 halves B's reads through L2 for the
+// long n x d-output contractions, where every M tile reads all of B).
+template <int BN, int STG = kStages, int MT = 1>
 struct GemmLayout {
-  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr uint32_t A_TILE = kBM * kBK * 2;
+  static constexpr uint32_t A_BYTES = MT * A_TILE;
   static constexpr uint32_t B_BYTES = BN * kBK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t BAR_OFF = STG * STAGE;
@@ -40,6 +44,7 @@ struct GemmLayout {
   // one then overlaps the loads and MMAs of the other)
   static constexpr int MINB = (TOTAL <= 232448 / 2 && BN <= 256) ? 2 : 1;
   static_assert(2 * STG + 2 <= 16, "barriers below the tensor-memory slot");
+  static_assert(MT * BN <= 512, "accumulators within the tensor memory");
 };
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -56,12 +61,12 @@ __device__ __forceinline__ uint32_t operand_lo(uint32_t base, bool kmajor, int k
   return kmajor ? sdesc_lo(base + kk * 32, 16) : sdesc_lo(base + kk * 2048, mn_block_bytes);
 }
 
-template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages, bool TMA_C = true>
-__global__ void __launch_bounds__(128, GemmLayout<BN, STG>::MINB)
+template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages, bool TMA_C = true, int MT = 1>
+__global__ void __launch_bounds__(128, GemmLayout<BN, STG, MT>::MINB)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                  const __grid_constant__ CUtensorMap tC, void* __restrict__ C, int M, int N, int K,
                  float alpha, KernelCtl ctl) {
-  using L = GemmLayout<BN, STG>;
+  using L = GemmLayout<BN, STG, MT>;
   constexpr int kStages = STG;   // ring depth of this instance
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -75,7 +80,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 136);
 
   const int warp = warp_id_uniform(), lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN, b = blockIdx.z;
+  const int m0 = blockIdx.y * (kBM * MT), n0 = blockIdx.x * BN, b = blockIdx.z;
   const int nkb = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -90,7 +95,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
     tma_prefetch_desc(&tA);
     tma_prefetch_desc(&tB);
   }
-  if (warp == 2) tmem_alloc<BN>(smem_u32(tmem_slot));
+  if (warp == 2) tmem_alloc<BN * MT>(smem_u32(tmem_slot));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -105,11 +110,16 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
       if (!mbar_wait(empty(s), ((kb / kStages) & 1) ^ 1, abort_flag, ctl, SITE_GEMM_EMPTY)) break;
       const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
       mbar_expect_tx(full(s), L::STAGE);
-      if (A_K) {
-        tma_load_3d(sa, &tA, kb * kBK, m0, b, full(s));
-      } else {
-        tma_load_3d(sa, &tA, m0, kb * kBK, b, full(s));
-        tma_load_3d(sa + 8192, &tA, m0 + 64, kb * kBK, b, full(s));
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {   // rows beyond M read the fill value
+        const uint32_t sat = sa + t * L::A_TILE;
+        const int mt = m0 + t * kBM;
+        if (A_K) {
+          tma_load_3d(sat, &tA, kb * kBK, mt, b, full(s));
+        } else {
+          tma_load_3d(sat, &tA, mt, kb * kBK, b, full(s));
+          tma_load_3d(sat + 8192, &tA, mt + 64, kb * kBK, b, full(s));
+        }
       }
       if (B_K) {
         tma_load_3d(sb, &tB, kb * kBK, n0, b, full(s));
@@ -136,14 +146,17 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
       if (!mbar_wait_warp(full(s), (kb / kStages) & 1, abort_flag, ctl, SITE_GEMM_FULL)) break;
       tc_fence_after();
       const uint32_t sa = sbase + s * L::STAGE, sb = sa + L::A_BYTES;
-      // the block's four K slices from one asm block
-      uint32_t alo[4], blo[4];
+      // the block's four K slices from one asm block per M tile
+      uint32_t blo[4];
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        alo[kk] = operand_lo(sa, A_K, kk, 8192);
-        blo[kk] = operand_lo(sb, B_K, kk, 8192);
+      for (int kk = 0; kk < kBK / 16; ++kk) blo[kk] = operand_lo(sb, B_K, kk, 8192);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        uint32_t alo[4];
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) alo[kk] = operand_lo(sa + t * L::A_TILE, A_K, kk, 8192);
+        mma_ss_x4(tmem + t * BN, alo, sdesc_hi(1024), blo, sdesc_hi(1024), idesc, kb != 0);
       }
-      mma_ss_x4(tmem, alo, sdesc_hi(1024), blo, sdesc_hi(1024), idesc, kb != 0);
       tc_commit(empty(s));
     }
     tc_commit(acc_bar);
@@ -170,8 +183,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
     constexpr int NBOX = (int)((L::BAR_OFF / BOX) < 4 ? (L::BAR_OFF / BOX) : 4);
     static_assert(NBOX >= 2, "two staging boxes at least");
     const int r = warp * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
     int slot = 0;
+#pragma unroll 1
+    for (int t = 0; t < MT && m0 + t * kBM < M; ++t) {
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + t * BN;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN && n0 + c0 < N; c0 += COLS) {
       uint32_t w[32];
@@ -202,16 +217,19 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (threadIdx.x == 0) {
-        tma_store_3d(&tC, smem_u32(box), n0 + c0, m0, b);
+        tma_store_3d(&tC, smem_u32(box), n0 + c0, m0 + t * kBM, b);
         bulk_commit_group();
       }
       slot = (slot + 1 == NBOX) ? 0 : slot + 1;
     }
+    }
     if (threadIdx.x == 0) bulk_wait_all();   // the stores are complete before the CTA exits
   }
   if (!TMA_C && ok) {
-    const int row = m0 + warp * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int t = 0; t < MT; ++t) {
+    const int row = m0 + t * kBM + warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + t * BN;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       uint32_t r[32];
@@ -249,15 +267,24 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__
         }
       }
     }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc<BN>(tmem);
+  if (warp == 2) tmem_dealloc<BN * MT>(tmem);
 }
 
-template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages>
+template <int BN, bool A_K, bool B_K, bool C_F32, int STG = kStages, int MT = 1>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int batch, int M,
                    int N, int K, float alpha, const KernelCtl& ctl, cudaStream_t st) {
+  // long contractions with n x d bf16 outputs (dQ = dS K and the other
+  // products against an n x n operand): two M tiles per CTA share each
+  // staged B block, which halves B's reads through L2 (every M tile reads
+  // all of B); three stages of 64 KB
+  if constexpr (STG == kStages && MT == 1 && BN == 256 && !C_F32) {
+    if (K > 4 * kBK && M > kBM)
+      return launch_variant<BN, A_K, B_K, C_F32, 3, 2>(ta, tb, C, batch, M, N, K, alpha, ctl, st);
+  }
   // short contractions (the n x n score products, K = d <= 256: four K blocks
   // or fewer) need no deep ring; two stages let two CTAs share an SM so that
   // one CTA's stores of its fp32 tile overlap the other's MMAs
@@ -272,12 +299,12 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int ba
       (C_F32 ? make_tmap_f32(&tc, C, N, M, batch, 32, kBM, true)
              : make_tmap_bf16(&tc, C, N, M, batch, 64, kBM));
   if (!tma_c) tc = ta;   // not read
-  auto kern = tma_c ? gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, true>
-                    : gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, false>;
-  constexpr int smem = GemmLayout<BN, STG>::TOTAL;
+  auto kern = tma_c ? gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, true, MT>
+                    : gemm_bf16_kernel<BN, A_K, B_K, C_F32, STG, false, MT>;
+  constexpr int smem = GemmLayout<BN, STG, MT>::TOTAL;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  dim3 grid(ceil_div(N, BN), ceil_div(M, kBM), batch);
+  dim3 grid(ceil_div(N, BN), ceil_div(M, kBM * MT), batch);
   kern<<<grid, 128, smem, st>>>(ta, tb, tc, C, M, N, K, alpha, ctl);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

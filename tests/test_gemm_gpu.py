@@ -62,3 +62,20 @@ def test_gemm_ragged_epilogues(cuda_dev, M, N, c_f32):
     attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, 1, 1)
     assert attn.attn_status() == 0
     assert relerr(c, ref) <= (1e-5 if c_f32 else 1e-2)
+
+
+@pytest.mark.parametrize("M,N,ak,bk", [(300, 260, 1, 1), (300, 264, 1, 1), (129, 256, 1, 1),
+                                       (264, 264, 0, 0), (264, 264, 1, 0)])
+def test_gemm_two_m_tiles(cuda_dev, M, N, ak, bk):
+    # long contractions with bf16 outputs and N > 128 run two 128-row M tiles
+    # per CTA against the same staged B block: a second tile that is partly
+    # or wholly past M, C rows through TMA tile stores (N * 2 bytes a
+    # multiple of 16) or direct stores, and MN-major operands
+    from io_aware_exact_05_gb300 import attn
+
+    batch, K = 2, 320
+    a, b, ref = _operands(batch, M, N, K, ak, bk, seed=M * 3 + N + ak + 2 * bk)
+    c = torch.full((batch, M, N), float("nan"), device=cuda_dev, dtype=torch.bfloat16)
+    attn.attn_gemm_bf16(a.to(cuda_dev), b.to(cuda_dev), c, batch, M, N, K, ak, bk, alpha=0.25)
+    assert attn.attn_status() == 0
+    assert relerr(c, 0.25 * ref) <= 1e-2
