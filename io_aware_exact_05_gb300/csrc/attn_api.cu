@@ -37,7 +37,7 @@ constexpr size_t kSpillAutoMaxBytes = size_t(4) << 30;
 // dQ mode actually used for a bf16 shape (measured choices).  d <= 128: the
 // key-tile kernel's reduce-adds (1.21-1.38 x faster than the pass).  d = 256:
 // the key-tile kernel has no tensor-memory columns for a dQ tile; the spill
-// mode (dS^T through the workspace, one GEMM) takes 19 % less time than the pass
+// mode (dS^T through the workspace, one GEMM) takes 21 % less time than the pass
 // where it applies (non-causal, dense, one key/value head per query head)
 // and while its n x n buffer stays under kSpillAutoMaxBytes; else the pass.
 attn_dq_mode resolve_mode(int B, int H, int H_kv, int n, int d, int causal, bool masked,
