@@ -102,11 +102,22 @@ struct KvCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// K_DSS (dQ mode "spill", one per dO slot): the compute warps have staged
-// dS^T of the tile in that slot for the TMA store.
-// K_DPF: one per dO slot (in the dK CTA's pass mode the dO slot is free once
-// dP^T is).  K_PR: one per Q slot (in the dV CTA the Q slot is free once the
-// compute warps have read S^T).
+// Barriers (every waiter waits on consecutive phases from phase 0, and the
+// phase after the one it waits for cannot complete before its own next
+// action):
+//   K_KV        K (and, in the dK CTA, V) loaded;  K_CP  K copied into TMEM
+//   K_QF/K_OF   Q / dO slot full (TMA, with the slot's row statistics)
+//   K_QE        dK CTA: Q slot free (committed after dK)
+//   K_PR        dV CTA: P^T in TMEM (one per Q slot, which it also frees)
+//   K_OE        dO slot free: dV CTA after dV; dK CTA in the dQ mode "spill"
+//               after the dS^T staged there has been stored
+//   K_SF/K_SF1  S^T slot full (the dK CTA uses K_SF only)
+//   K_SC        dK CTA: the compute warps hold P in registers (S^T slot free)
+//   K_DPF       dK CTA: dP^T full (one per dO slot; in the pass mode it also
+//               frees the slot)
+//   K_DSR       dK CTA: dS^T in TMEM
+//   K_DSS       spill: dS^T staged in the dO slot for the TMA store
+//   K_ACC/K_DRAIN  all MMAs done (epilogue / abort drain)
 enum : int { K_KV = 0, K_QF = 1, K_QE = 4, K_OF = 7, K_OE = 9, K_SF = 11, K_SF1 = 12, K_DPF = 13,
              K_PR = 15, K_SC = 18, K_DSR = 19, K_ACC = 20, K_DRAIN = 21, K_CP = 22, K_DSS = 23 };
 
